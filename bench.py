@@ -1,0 +1,491 @@
+#!/usr/bin/env python
+"""Benchmark: KDA decode state-updates/s and HBM roofline fraction on GB300.
+
+One step = one kda_decode call (C ABI) over the large-batch grouped decode
+workload: B = 256 requests x 1 token, key heads H = 48, value heads HV = 96
+(G = 2), dk = dv = 128, state pool [512, 96, 128, 128] fp32 (3.2 GB, far
+larger than L2, so no flush is needed between steps), softplus gate.  The
+state pool is advanced in place step after step (bounded: beta <= 1, unit
+keys, exp(g) <= 1).
+
+Printed (rank 0, one JSON line): state-updates/s (req x head x token), the
+decode kernel's roofline against the measured HBM copy bandwidth, an
+end-to-end figure through host buffers, SM clocks sampled during the timed
+region, the float64 oracle timed on the host cores, and the fused block
+(kda_block_tkg, B = 32, Hd = 4096, nh = 32) timed separately.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from kda_decode_recurrence_gb300.inputs import (BLOCK_CONFIG, DECODE_CONFIGS,  # noqa: E402
+                                                block_inputs, decode_inputs, to_f64)
+
+METRIC = "KDA decode state-updates/s (req·head·token) and HBM GB/s vs GB300 peak"
+UNIT = "state-updates/s"
+WORKLOAD = "grouped"
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes per launch of the decode kernel from one ncu capture (see
+# profiles/), tied to the kernel sources they were taken with: when the
+# sources change the figure no longer describes the kernel and is reported
+# as null.
+NCU_TRAFFIC = {"sources_sha256": None, "bytes_per_launch": None}
+
+
+def kernel_sources_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "kda_decode_recurrence_gb300", "csrc")
+    for f in ("kda_common.cuh", "kda_recurrence.cuh", "kda_decode.cu"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def decode_bytes(B, T, H, HV, K, V, touched=None) -> int:
+    """Algorithmic HBM bytes of one kda_decode call: each advanced state tile
+    read and written once, q/k once per key head (bf16), v (bf16), raw_gate,
+    beta_logits, output (fp32), a_log, dt_bias, cu_seqlens, state_indices."""
+    touched = B if touched is None else touched
+    return (touched * HV * 2 * K * V * 4
+            + T * (H * K * 2 * 2 + HV * V * 2 + HV * K * 4 + HV * 4 + HV * V * 4)
+            + HV * (K + 1) * 4 + (2 * B + 1) * 4)
+
+
+def block_bytes(B, Hd, nh, K, V, Kc) -> int:
+    """Algorithmic HBM bytes of one kda_block_tkg call (n = 1): weights once,
+    S and conv_state read + written, hidden in, out out, small parameters."""
+    I = 2 * K * nh + V * nh + 2 * K + nh
+    weights = 2 * (Hd * I + K * K * nh + K * V * nh + 3 * Kc * K * nh + V * nh * Hd)
+    params = 4 * (Hd + nh + K * nh + V)
+    state = B * nh * K * V * 4 * 2 + B * 3 * K * nh * (Kc - 1) * 4 * 2
+    io = B * Hd * 4 * 2
+    return weights + params + state + io
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
+
+    QUERY = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            if self.uuid and parts[0] != self.uuid:
+                continue
+            self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        if not inside and self.samples:  # region shorter than one sample period
+            nearest = min(self.samples, key=lambda s: abs(s[0] - (t0 + t1) / 2))
+            inside = [nearest[1]]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        smax = [num(p[2]) for p in inside if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(inside)}
+
+
+def device_uuid():
+    try:
+        u = str(torch.cuda.get_device_properties(0).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """The slowest rank's time: the job's time."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def shard_seed(base_seed: int, rank: int) -> int:
+    """Each rank draws its own batch (own requests, own pool slots): weak scaling."""
+    return base_seed + 1000 * rank
+
+
+# ----------------------------------------------------------------- oracle
+
+
+def oracle_rate(inp: dict, n_requests: int):
+    """Time the float64 oracle on the first n_requests requests of a decode
+    workload (all value heads).  Returns (state-updates/s, seconds, updates)."""
+    import oracle
+    cu = inp["cu_seqlens"].numpy()
+    idx = inp["state_indices"].numpy()[:n_requests].astype(np.int64)
+    rows = np.arange(cu[0], cu[n_requests])
+    tok = {k: to_f64(inp[k][torch.from_numpy(rows)]) for k in ("q", "k", "v", "raw_gate",
+                                                                 "beta_logits")}
+    pool = to_f64(inp["state_pool"][torch.from_numpy(idx)])
+    a_log, dt_bias = to_f64(inp["a_log"]), to_f64(inp["dt_bias"])
+    cu_s = (cu[:n_requests + 1] - cu[0]).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.kda_decode(tok["q"], tok["k"], tok["v"], tok["raw_gate"], tok["beta_logits"], a_log,
+                      dt_bias, cu_s, pool, np.arange(n_requests), gate_mode=inp["gate_mode"],
+                      lower_bound=inp["lower_bound"])
+    dt = time.perf_counter() - t0
+    updates = len(rows) * inp["HV"]
+    return updates / dt, dt, updates
+
+
+def cpu_baseline(inp: dict, budget_s: float = 12.0) -> dict:
+    rate1, dt1, _ = oracle_rate(inp, 2)
+    n = int(max(2, min(inp["B"], budget_s / max(dt1 / 2, 1e-6))))
+    rate, dt, upd = oracle_rate(inp, n)
+    return {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} of {inp['B']} requests x {inp['HV']} value heads ({upd} state updates, "
+                      f"{dt:.1f} s, float64 C oracle, single thread)"}
+
+
+def config_dict(cfg) -> dict:
+    return {"workload": f"{cfg.name} decode: B={cfg.B} x 1 token, H={cfg.H}, HV={cfg.HV} "
+                        f"(G={cfg.HV // cfg.H}), dk=dv={cfg.K}, state_pool [{cfg.max_slots}, {cfg.HV}, "
+                        f"{cfg.K}, {cfg.V}] fp32, softplus gate",
+            "B": cfg.B, "T": cfg.B, "H": cfg.H, "HV": cfg.HV, "K": cfg.K, "V": cfg.V,
+            "max_slots": cfg.max_slots, "gate_mode": "softplus", "seed": cfg.seed,
+            "l2": "no flush: the 3.2 GB state pool is larger than L2 (129 MB)"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the float64 oracle on the host cores."""
+    if rank != 0:
+        return
+    cfg = DECODE_CONFIGS[WORKLOAD]
+    inp = decode_inputs(cfg)
+    _, dt2, _ = oracle_rate(inp, 2)
+    per_req = dt2 / 2
+    total = args.steps + args.warmup
+    n = int(max(1, min(cfg.B, 150.0 / max(total, 1) / max(per_req, 1e-6))))
+    for _ in range(args.warmup):
+        oracle_rate(inp, n)
+    times, upd = [], 0
+    for _ in range(args.steps):
+        _, dt, u = oracle_rate(inp, n)
+        times.append(dt)
+        upd = u
+    elapsed = sum(times)
+    value = upd * args.steps / elapsed
+    sample = (f"each step: {n} of {cfg.B} requests x {cfg.HV} value heads ({upd} state updates), "
+              "float64 C oracle, single thread")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * elapsed / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(cfg),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------- GPU arm
+
+
+def run_block(steps: int, warmup: int) -> dict:
+    from kda_decode_recurrence_gb300 import block_workspace_size, kda_block_tkg
+    cfg = BLOCK_CONFIG
+    inp = block_inputs(cfg)
+    dev = "cuda"
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    out = torch.empty(cfg.B, cfg.n, cfg.Hd, device=dev)
+    ws = torch.empty(block_workspace_size(cfg.B, cfg.n, cfg.Hd, cfg.nh, cfg.K, cfg.V, cfg.Kc),
+                     dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    names = ("hidden", "gamma_in", "W_in", "W_fb", "W_gb", "conv_w", "A_log", "dt_bias",
+             "gamma_o", "W_o")
+
+    def call():
+        kda_block_tkg(out, *[d[k] for k in names], d["S"], d["conv_state"], inp["scale"],
+                      inp["lower_bound"], inp["rms_norm_eps"], inp["l2_eps"], workspace=ws)
+
+    for _ in range(warmup):
+        call()
+    stream = torch.cuda.current_stream()
+    times = []
+    for _ in range(steps):
+        flush.fill_(1)  # evict L2 between calls
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        call()
+        e.record(stream)
+        e.synchronize()
+        times.append(s.elapsed_time(e) * 1e-3)
+    t = statistics.median(times)
+    nbytes = block_bytes(cfg.B, cfg.Hd, cfg.nh, cfg.K, cfg.V, cfg.Kc)
+    peak, src = measured_peaks()
+    return {"workload": f"kda_block_tkg B={cfg.B} n=1 Hd={cfg.Hd} nh={cfg.nh} dk=dv={cfg.K} "
+                        f"Kc={cfg.Kc}, L2 flushed before each call",
+            "us_per_call": t * 1e6, "calls": steps, "gpu_launches_per_call": 6,
+            "algorithmic_bytes": nbytes, "achieved_gbs": nbytes / t / 1e9,
+            "frac_of_hbm_peak": nbytes / t / 1e9 / peak, "peak_source": src,
+            "state_updates_per_s": cfg.B * cfg.nh / t}
+
+
+def run_gpu(args, rank, world, local):
+    from kda_decode_recurrence_gb300 import kda_decode
+    cfg = DECODE_CONFIGS[WORKLOAD]
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inp = decode_inputs(cfg, seed=shard_seed(cfg.seed, rank))
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    B, T, H, HV, K, V = inp["B"], inp["T"], inp["H"], inp["HV"], inp["K"], inp["V"]
+    out = torch.empty(T, HV, V, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda_decode(out, d["q"], d["k"], d["v"], d["raw_gate"], d["beta_logits"], d["a_log"],
+                   d["dt_bias"], d["cu_seqlens"], d["state_pool"], d["state_indices"],
+                   gate_mode=inp["gate_mode"], lower_bound=inp["lower_bound"], stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(device_uuid())
+    sampler.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    w0 = time.time()
+    for s, e in ev:
+        s.record(stream)
+        step()
+        e.record(stream)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    w1 = time.time()
+    time.sleep(0.25)
+    sampler.stop()
+    clocks = sampler.summary(w0, w1)
+
+    elapsed = ev[0][0].elapsed_time(ev[-1][1]) * 1e-3
+    kernel_times = [s.elapsed_time(e) * 1e-3 for s, e in ev]
+    kernel_avg = sum(kernel_times) / len(kernel_times)
+    elapsed_max = max_over_ranks(elapsed, world)
+    updates_per_step = T * HV
+    value = world * updates_per_step * args.steps / elapsed_max
+
+    # end to end through the C ABI with host buffers: pinned inputs copied in,
+    # the output copied back, every step.
+    host = {k: inp[k].pin_memory() for k in ("q", "k", "v", "raw_gate", "beta_logits",
+                                              "cu_seqlens", "state_indices")}
+    dev_in = {k: torch.empty_like(host[k], device=dev) for k in host}
+    host_out = torch.empty(T, HV, V, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for k in host:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        kda_decode(out, dev_in["q"], dev_in["k"], dev_in["v"], dev_in["raw_gate"],
+                   dev_in["beta_logits"], d["a_log"], d["dt_bias"], dev_in["cu_seqlens"],
+                   d["state_pool"], dev_in["state_indices"], gate_mode=inp["gate_mode"],
+                   lower_bound=inp["lower_bound"], stream=stream)
+        host_out.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    e2e_steps = max(3, min(args.steps, 200))
+    for _ in range(3):
+        e2e_step()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    es.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    ee.record(stream)
+    ee.synchronize()
+    e2e_elapsed = max_over_ranks(es.elapsed_time(ee) * 1e-3, world)
+    e2e_value = world * updates_per_step * e2e_steps / e2e_elapsed
+
+    block = run_block(steps=max(5, min(args.steps, 50)), warmup=3) if rank == 0 else None
+
+    if rank != 0:
+        return
+    nbytes = decode_bytes(B, T, H, HV, K, V)
+    peak, peak_src = measured_peaks()
+    achieved = nbytes / kernel_avg / 1e9
+    traffic = None
+    if NCU_TRAFFIC["sources_sha256"] == kernel_sources_sha():
+        traffic = NCU_TRAFFIC["bytes_per_launch"]
+    cpu = cpu_baseline(inp) if world == 1 else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * elapsed_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded numpy PCG64; bf16 q/k/v, fp32 gates/state)",
+        "config": config_dict(cfg),
+        "output_tokens_per_s": world * T * args.steps / elapsed_max,
+        "hbm_gbs": nbytes / (elapsed_max / args.steps) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                     else "fallback 6800 GB/s", "algorithmic_bytes_per_launch": nbytes,
+                     "kernel": "kda_decode_kernel", "kernel_avg_us": kernel_avg * 1e6},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "note": "pinned host q/k/v/raw_gate/beta_logits/cu_seqlens/state_indices in, "
+                        "output out, stream synchronised every step; state pool and model "
+                        "parameters resident on the device"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "block_tkg": block,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_profile_case(args, which: str):
+    """A reduced case for ncu captures: the decode kernel on B = 32 requests x
+    1 token, H = 48, HV = 96 (a 64-slot, 400 MB pool; 200 MB of state traffic
+    per launch, above the L2 size), or the block at its full size.  Prints
+    the median kernel time only."""
+    from kda_decode_recurrence_gb300 import kda_decode
+    dev = torch.device("cuda", 0)
+    if which == "block":
+        print(json.dumps({"profile": "block", **run_block(args.steps, args.warmup)}))
+        return
+    inp = decode_inputs(DECODE_CONFIGS[WORKLOAD], B=32, max_slots=64)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    out = torch.empty(inp["T"], inp["HV"], inp["V"], device=dev)
+    times = []
+    for i in range(args.warmup + args.steps):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        kda_decode(out, d["q"], d["k"], d["v"], d["raw_gate"], d["beta_logits"], d["a_log"],
+                   d["dt_bias"], d["cu_seqlens"], d["state_pool"], d["state_indices"],
+                   gate_mode=inp["gate_mode"], lower_bound=inp["lower_bound"])
+        e.record()
+        e.synchronize()
+        if i >= args.warmup:
+            times.append(s.elapsed_time(e) * 1e-3)
+    t = statistics.median(times)
+    nbytes = decode_bytes(inp["B"], inp["T"], inp["H"], inp["HV"], inp["K"], inp["V"])
+    print(json.dumps({"profile": "decode", "B": inp["B"], "us": t * 1e6,
+                      "algorithmic_bytes": nbytes, "gbs": nbytes / t / 1e9}))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--profile", choices=["decode", "block"], default=None,
+                    help="run a reduced case of one kernel for ncu (no JSON bench line)")
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="kda", choices=["kda", "reference"])
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    args.steps = max(args.steps, 1)
+    if args.profile:
+        run_profile_case(args, args.profile)
+        return
+    rank, world, local = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_gpu(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

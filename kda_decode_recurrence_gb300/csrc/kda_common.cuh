@@ -1,0 +1,34 @@
+// kda_common.cuh -- small device helpers shared by the libkda kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+#include "kda_internal.h"
+
+namespace kda {
+
+// bf16 bit patterns -> fp32 (exact: a bf16 is the top half of an fp32).
+__device__ __forceinline__ float bf16_lo(uint32_t pair) { return __uint_as_float(pair << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t pair) { return __uint_as_float(pair & 0xffff0000u); }
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+  return x;
+}
+
+// 1 / (1 + e^-x) through the correctly rounded reciprocal intrinsic (no
+// divide slow path; e^-x = inf gives exactly 0).
+__device__ __forceinline__ float sigmoidf_(float x) { return __frcp_rn(1.0f + expf(-x)); }
+
+// log(1 + e^x) without overflow: max(x, 0) + log1p(e^-|x|).
+__device__ __forceinline__ float softplusf_(float x) { return fmaxf(x, 0.0f) + log1pf(expf(-fabsf(x))); }
+
+__device__ __forceinline__ void raise_status(int32_t* status, int32_t bit) {
+  if (status != nullptr) atomicOr(status, bit);
+}
+
+}  // namespace kda

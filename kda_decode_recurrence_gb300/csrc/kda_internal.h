@@ -1,0 +1,62 @@
+// kda_internal.h -- argument bundles passed from the C ABI layer to the
+// kernel launchers (host and device visible; no allocation, no ownership).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+// Head dimension this build implements (the block API page allows dk, dv <=
+// 128; the Kimi K3 atlas page gives 128).
+constexpr int kHeadDim = 128;
+
+struct DecodeArgs {
+  float* output;
+  const kda_bf16* q;
+  const kda_bf16* k;
+  const kda_bf16* v;
+  const float* raw_gate;
+  const float* beta_logits;
+  const float* a_log;
+  const float* dt_bias;
+  const int32_t* cu_seqlens;
+  float* state_pool;
+  const int32_t* state_indices;
+  int32_t* dev_status;
+  int gate_mode;
+  float lower_bound;
+  float q_scale;  // K^-1/2
+  int B, T, H, HV, G, max_slots;
+};
+
+cudaError_t launch_kda_decode(const DecodeArgs& args, cudaStream_t stream);
+
+struct BlockArgs {
+  float* out;
+  const float* hidden;
+  const float* gamma_in;
+  const kda_bf16* W_in;
+  const kda_bf16* W_fb;
+  const kda_bf16* W_gb;
+  const kda_bf16* conv_w;
+  const float* A_log;
+  const float* dt_bias;
+  const float* gamma_o;
+  const kda_bf16* W_o;
+  float* S;
+  float* conv_state;
+  float scale, lower_bound, rms_norm_eps, l2_eps;
+  int B, n, Hd, nh, K, V, Kc;
+  void* workspace;
+  size_t workspace_bytes;
+  int32_t* dev_status;
+};
+
+size_t block_workspace_bytes(int B, int n, int Hd, int nh, int K, int V, int Kc);
+cudaError_t launch_kda_block(const BlockArgs& args, cudaStream_t stream);
+
+}  // namespace kda

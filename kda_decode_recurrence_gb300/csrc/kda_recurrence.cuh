@@ -1,0 +1,94 @@
+// kda_recurrence.cuh -- the register-resident delta-rule step on one fp32
+// [128, 128] state tile, shared by the decode kernel and the block's head
+// kernel.
+//
+// Tile ownership inside a 256-thread CTA: warp w owns value columns
+// [16w, 16w + 16); lane = 4 * rg + cg holds rows rg, rg + 8, ..., rg + 120 of
+// the four columns 16w + 4cg .. 16w + 4cg + 3, i.e. 16 float4 registers.  A
+// warp's load/store instruction i covers rows 8i .. 8i + 7 x 64 contiguous
+// bytes.
+//
+// One token ("Delta-rule write", naive recurrent loop; decay, delta write,
+// read after the write):
+//   S <- diag(exp(g)) S;  u = v - kh^T S;  S <- S + beta kh u^T;  o = qh^T S.
+// The read is taken as qh^T S = qh^T (D S_old) + beta (qh . kh) u, the same
+// quantity with a single pass over the tile.
+#pragma once
+
+#include "kda_common.cuh"
+
+namespace kda {
+
+struct __align__(16) RowCoef {
+  float decay;  // exp(g[k])
+  float kh;     // normalised key
+  float qh;     // normalised, scaled query
+  float bkh;    // beta * kh
+};
+
+// Per-token vectors in shared memory.
+struct __align__(16) TokenStage {
+  RowCoef row[kHeadDim];
+  float v[kHeadDim];
+  float bqk;  // beta * (qh . kh)
+  float pad[3];
+};
+
+struct TileLane {
+  int rg;   // row group 0..7
+  int col;  // first of the lane's four value columns
+};
+
+__device__ __forceinline__ TileLane tile_lane() {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  return TileLane{lane >> 2, warp * 16 + (lane & 3) * 4};
+}
+
+__device__ __forceinline__ void tile_load(float4 (&s)[16], const float* tile, TileLane tl) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    s[i] = __ldcs(reinterpret_cast<const float4*>(tile + (tl.rg + 8 * i) * kHeadDim + tl.col));
+}
+
+__device__ __forceinline__ void tile_store(float* tile, const float4 (&s)[16], TileLane tl) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    __stcs(reinterpret_cast<float4*>(tile + (tl.rg + 8 * i) * kHeadDim + tl.col), s[i]);
+}
+
+// Advance the tile by one token; returns the read o for the lane's columns
+// (identical in the 8 lanes of a column quad).
+__device__ __forceinline__ float4 tile_token_step(float4 (&s)[16], const TokenStage& ts,
+                                                  TileLane tl) {
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const RowCoef rc = ts.row[tl.rg + 8 * i];
+    s[i].x *= rc.decay; s[i].y *= rc.decay; s[i].z *= rc.decay; s[i].w *= rc.decay;
+    a.x = fmaf(rc.kh, s[i].x, a.x); a.y = fmaf(rc.kh, s[i].y, a.y);
+    a.z = fmaf(rc.kh, s[i].z, a.z); a.w = fmaf(rc.kh, s[i].w, a.w);
+    c.x = fmaf(rc.qh, s[i].x, c.x); c.y = fmaf(rc.qh, s[i].y, c.y);
+    c.z = fmaf(rc.qh, s[i].z, c.z); c.w = fmaf(rc.qh, s[i].w, c.w);
+  }
+#pragma unroll
+  for (int m = 4; m < 32; m <<= 1) {
+    a.x += __shfl_xor_sync(0xffffffffu, a.x, m); a.y += __shfl_xor_sync(0xffffffffu, a.y, m);
+    a.z += __shfl_xor_sync(0xffffffffu, a.z, m); a.w += __shfl_xor_sync(0xffffffffu, a.w, m);
+    c.x += __shfl_xor_sync(0xffffffffu, c.x, m); c.y += __shfl_xor_sync(0xffffffffu, c.y, m);
+    c.z += __shfl_xor_sync(0xffffffffu, c.z, m); c.w += __shfl_xor_sync(0xffffffffu, c.w, m);
+  }
+  const float4 vv = *reinterpret_cast<const float4*>(&ts.v[tl.col]);
+  const float4 u = make_float4(vv.x - a.x, vv.y - a.y, vv.z - a.z, vv.w - a.w);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float bkh = ts.row[tl.rg + 8 * i].bkh;
+    s[i].x = fmaf(bkh, u.x, s[i].x); s[i].y = fmaf(bkh, u.y, s[i].y);
+    s[i].z = fmaf(bkh, u.z, s[i].z); s[i].w = fmaf(bkh, u.w, s[i].w);
+  }
+  const float bqk = ts.bqk;
+  return make_float4(fmaf(bqk, u.x, c.x), fmaf(bqk, u.y, c.y), fmaf(bqk, u.z, c.z),
+                     fmaf(bqk, u.w, c.w));
+}
+
+}  // namespace kda

@@ -1,0 +1,156 @@
+"""kda_decode on the GPU (through the C ABI) against the float64 oracle.
+
+Full-size workloads (single, grouped, varlen) run in the launch configuration
+the benchmark times; the oracle checks a sample of their requests one by one,
+and the untouched part of the pool is compared bit for bit.  Small and ragged
+cases are compared in full.
+"""
+import numpy as np
+import pytest
+import torch
+
+from kda_decode_recurrence_gb300 import DEV_BAD_SEQLEN, DEV_BAD_SLOT, GATE_LOWER_BOUND, kda_decode
+from kda_decode_recurrence_gb300.inputs import decode_inputs, to_f64
+
+from _parity import (assert_outputs_close, assert_states_close, gpu_decode,
+                     oracle_decode_sample, to_device)
+
+pytestmark = pytest.mark.gpu
+
+
+def check_all(inp, bs=None):
+    out, pool, st = gpu_decode(inp)
+    assert st == 0
+    B = inp["B"]
+    bs = list(range(B)) if bs is None else bs
+    rows, slots, ref_out, ref_pool = oracle_decode_sample(inp, bs)
+    assert_outputs_close(out.cpu().numpy()[rows], ref_out)
+    assert_states_close(pool[torch.from_numpy(slots.astype(np.int64))].cpu().numpy(), ref_pool)
+    return out, pool
+
+
+def test_tiny_full():
+    check_all(decode_inputs("tiny"))
+
+
+@pytest.mark.parametrize("name", ["single", "grouped", "varlen"])
+def test_full_size_sampled(name):
+    inp = decode_inputs(name)
+    rng = np.random.default_rng(1234)
+    B = inp["B"]
+    bs = sorted(set([0, B - 1] + rng.choice(B, size=14, replace=False).tolist()))
+    d = to_device(inp)
+    before = d["state_pool"].clone()
+    out = torch.full((inp["T"], inp["HV"], inp["V"]), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda_decode(out, d["q"], d["k"], d["v"], d["raw_gate"], d["beta_logits"], d["a_log"],
+               d["dt_bias"], d["cu_seqlens"], d["state_pool"], d["state_indices"],
+               gate_mode=inp["gate_mode"], lower_bound=inp["lower_bound"], dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert torch.isfinite(out).all().item()          # every token row written
+    rows, slots, ref_out, ref_pool = oracle_decode_sample(inp, bs)
+    assert_outputs_close(out[torch.from_numpy(rows).cuda()].cpu().numpy(), ref_out)
+    assert_states_close(d["state_pool"][torch.from_numpy(slots.astype(np.int64)).cuda()].cpu().numpy(),
+                        ref_pool)
+    used = torch.zeros(inp["max_slots"], dtype=torch.bool, device="cuda")
+    used[d["state_indices"].long()] = True
+    assert torch.equal(d["state_pool"][~used], before[~used])   # untouched slots bit-identical
+    assert not torch.equal(d["state_pool"][used], before[used])
+
+
+@pytest.mark.parametrize("gate", [0, 1])
+@pytest.mark.parametrize("H,HV", [(3, 6), (2, 2), (1, 4)])
+def test_ragged_varlen_small(gate, H, HV):
+    # lengths include an empty request, one token, more than one staging round
+    # (> 8 tokens) and a ragged last round
+    lengths = (0, 1, 9, 17, 3)
+    inp = decode_inputs("varlen", B=5, H=H, HV=HV, max_slots=11, lengths=lengths, seed=40 + gate)
+    inp["gate_mode"] = gate
+    out, pool = check_all(inp, bs=[1, 2, 3, 4])
+    empty_slot = int(inp["state_indices"][0])
+    assert torch.equal(pool[empty_slot].cpu(), inp["state_pool"][empty_slot])
+
+
+def test_padded_and_out_of_range_slots():
+    inp = decode_inputs("varlen", B=4, H=2, HV=4, max_slots=6, lengths=(2, 1, 3, 2), seed=50)
+    inp["state_indices"] = torch.tensor([3, -1, 1, 6], dtype=torch.int32)  # 6 == max_slots: bad
+    out, pool, st = gpu_decode(inp)
+    assert st == DEV_BAD_SLOT
+    cu = inp["cu_seqlens"].numpy()
+    o = out.cpu().numpy()
+    assert np.all(o[cu[1]:cu[2]] == 0.0) and np.all(o[cu[3]:cu[4]] == 0.0)
+    for s in (0, 2, 4, 5):
+        assert torch.equal(pool[s].cpu(), inp["state_pool"][s])
+    rows, slots, ref_out, ref_pool = oracle_decode_sample(inp, [0, 2])
+    assert_outputs_close(o[rows], ref_out)
+    assert_states_close(pool[torch.tensor(slots.astype(np.int64))].cpu().numpy(), ref_pool)
+
+
+@pytest.mark.parametrize("cu", [[0, 3, 2, 6], [0, 2, 4, 7], [1, 2, 4, 6]])
+def test_malformed_cu_seqlens_flagged(cu):
+    inp = decode_inputs("varlen", B=3, H=2, HV=2, max_slots=4, lengths=(2, 2, 2), seed=51)
+    inp["cu_seqlens"] = torch.tensor(cu, dtype=torch.int32)
+    out, pool, st = gpu_decode(inp, output_fill=0.0)
+    assert st & DEV_BAD_SEQLEN
+
+
+def test_no_tokens_is_a_no_op():
+    inp = decode_inputs("varlen", B=3, H=2, HV=2, max_slots=4, lengths=(0, 0, 0), seed=52)
+    d = to_device(inp)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty(0, 2, 128, device="cuda")
+    kda_decode(out, d["q"], d["k"], d["v"], d["raw_gate"], d["beta_logits"], d["a_log"],
+               d["dt_bias"], d["cu_seqlens"], d["state_pool"], d["state_indices"],
+               dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert torch.equal(d["state_pool"].cpu(), inp["state_pool"])
+
+
+def test_multi_token_call_equals_single_token_calls():
+    inp = decode_inputs("varlen", B=4, H=2, HV=4, max_slots=5, lengths=(5, 1, 12, 3), seed=53)
+    out_all, pool_all, st = gpu_decode(inp)
+    assert st == 0
+    d = to_device(inp)
+    cu = inp["cu_seqlens"].tolist()
+    out_step = torch.empty_like(out_all)
+    for b in range(4):
+        for t in range(cu[b], cu[b + 1]):
+            o = torch.empty(1, 4, 128, device="cuda")
+            kda_decode(o, d["q"][t:t + 1], d["k"][t:t + 1], d["v"][t:t + 1],
+                       d["raw_gate"][t:t + 1], d["beta_logits"][t:t + 1], d["a_log"], d["dt_bias"],
+                       torch.tensor([0, 1], dtype=torch.int32, device="cuda"), d["state_pool"],
+                       d["state_indices"][b:b + 1].contiguous(), gate_mode=inp["gate_mode"],
+                       lower_bound=inp["lower_bound"])
+            out_step[t] = o[0]
+    torch.cuda.synchronize()
+    # the tile is stored in fp32 exactly as held on chip, so chaining calls is
+    # bit-identical to one call
+    assert torch.equal(out_step, out_all)
+    assert torch.equal(d["state_pool"], pool_all)
+
+
+def test_same_token_read_returns_value_at_full_size():
+    # beta = 1 and q = k: q^T S_new = K^-1/2 v for any state and gate (the
+    # delta-rule property), up to the l2_eps term (~1e-8 relative here).
+    inp = decode_inputs("grouped")
+    inp["q"] = inp["k"].clone()
+    inp["beta_logits"] = torch.full_like(inp["beta_logits"], 40.0)
+    out, _, st = gpu_decode(inp)
+    assert st == 0
+    expect = to_f64(inp["v"]) * 128 ** -0.5
+    err = np.abs(out.cpu().numpy() - expect)
+    assert err.max() <= 1e-4 * (1 + np.abs(expect)).max()
+
+
+def test_lower_bound_gate_never_amplifies_on_gpu():
+    inp = decode_inputs("varlen", B=8, H=4, HV=4, max_slots=8, lengths=(1,) * 8, seed=54)
+    inp["gate_mode"] = GATE_LOWER_BOUND
+    inp["beta_logits"] = torch.full_like(inp["beta_logits"], -200.0)   # beta == 0: decay only
+    inp["raw_gate"] = inp["raw_gate"] * 10
+    _, pool, st = gpu_decode(inp)
+    assert st == 0
+    slots = inp["state_indices"].long()
+    ratio = (pool[slots.cuda()].cpu() / inp["state_pool"][slots]).numpy()
+    assert np.all(ratio <= 1.0) and np.all(ratio >= np.exp(-5.0) * (1 - 1e-6))
