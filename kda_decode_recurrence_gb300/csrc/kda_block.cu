@@ -6,40 +6,35 @@
 // write".
 //
 // Kernel chain on the caller's stream (rows r = b, R = B):
-//   1. rmsnorm      x = hidden * rsqrt(mean(hidden^2) + eps) * gamma_in      [R, Hd]
-//   2. proj GEMM    P_part[ks] = x[:, chunk ks] . W_in[chunk ks, :]         [KS1, R, I]
-//                   (split-K over the hidden dimension so every SM streams a
-//                   slice of W_in; the partial sums are added by consumers)
-//   3. latent GEMM  graw = f_a . W_fb, z = g_a . W_gb                        [R, CQ + CV]
+//   1. rmsnorm      x = hidden * rsqrt(mean(hidden^2) + eps) * gamma_in, written
+//                   as bf16 hi/lo halves X2 [2R, Hd] for the tensor cores
+//   2. proj GEMM    tcgen05, P_part[ks] = x[:, split ks] . W_in[split ks, :]   [KS1, R, I]
+//                   (split-K so every SM streams a slice of the 103 MB W_in;
+//                   consumers add the KS1 partial sums)
+//   3. latent       graw = f_a . W_fb, z = g_a . W_gb (CUDA cores)            [R, CQ + CV]
 //   4. head         one CTA per (b, h): short conv + SiLU + conv_state update
 //                   for the head's q, k, v channels, forget gate, beta, L2
 //                   norms, the register-tile delta-rule step on S[b, h] (shared
-//                   with kda_decode), gated output RMSNorm -> on [R, nh*V]
-//   5. out GEMM     O_part[ks] = on[:, chunk ks] . W_o[chunk ks, :]          [KS2, R, Hd]
+//                   with kda_decode), gated output RMSNorm -> bf16 hi/lo on2
+//   5. out GEMM     tcgen05, O_part[ks] = on[:, split ks] . W_o[split ks, :]   [KS2, R, Hd]
 //   6. reduce       out = sum_ks O_part[ks]
-// Intermediates live in the caller's workspace (a few tens of MB: they stay
-// L2-resident on GB300).  The GEMMs accumulate in fp32 from fp32 activations
-// and exact bf16 weights on the CUDA cores.
+// Intermediates live in the caller's workspace (a few MB: L2-resident).
 #include "kda_recurrence.cuh"
+#include "kda_tc_gemm.h"
 
 namespace kda {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kGemmCols = 2 * kThreads;  // output columns per GEMM CTA (2 per thread)
-constexpr int kGemmRows = 32;            // rows (requests) per GEMM CTA
-constexpr int kGemmKSub = 16;            // contraction rows staged per sub-step
+constexpr int kLatCols = 64;   // latent GEMM: output columns per CTA
+constexpr int kLatRows = 32;   // latent GEMM: rows per CTA
+constexpr int kKS1 = 4;        // contraction splits of the W_in GEMM
+constexpr int kKS2 = 8;        // contraction splits of the W_o GEMM
 
 struct Layout {
-  int R, I, CQ, CV, KS1, KS2, kchunk1, kchunk2;
-  size_t xhat, ppart, gz, on, opart, total;
+  int R, I, CQ, CV, KS1, KS2;
+  size_t x2, ppart, gz, on2, opart, err, total;
 };
-
-int largest_divisor_at_most(int n, int cap) {
-  for (int d = cap; d > 1; --d)
-    if (n % d == 0) return d;
-  return 1;
-}
 
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -51,18 +46,24 @@ bool make_layout(int B, int n, int Hd, int nh, int K, int V, int Kc, Layout* L) 
   L->CQ = K * nh;
   L->CV = V * nh;
   L->I = 2 * L->CQ + L->CV + 2 * K + nh;
-  L->KS1 = largest_divisor_at_most(Hd / 128, 16);
-  L->kchunk1 = Hd / L->KS1;
-  L->KS2 = largest_divisor_at_most(L->CV / 128, 32);
-  L->kchunk2 = L->CV / L->KS2;
+  L->KS1 = Hd / 64 < kKS1 ? Hd / 64 : kKS1;        // splits <= 64-row contraction blocks
+  L->KS2 = L->CV / 64 < kKS2 ? L->CV / 64 : kKS2;
   size_t off = 0;
-  L->xhat = off;  off = align_up(off + sizeof(float) * (size_t)L->R * Hd);
+  L->x2 = off;    off = align_up(off + 2 * sizeof(kda_bf16) * (size_t)L->R * Hd);
   L->ppart = off; off = align_up(off + sizeof(float) * (size_t)L->KS1 * L->R * L->I);
   L->gz = off;    off = align_up(off + sizeof(float) * (size_t)L->R * (L->CQ + L->CV));
-  L->on = off;    off = align_up(off + sizeof(float) * (size_t)L->R * L->CV);
+  L->on2 = off;   off = align_up(off + 2 * sizeof(kda_bf16) * (size_t)L->R * L->CV);
   L->opart = off; off = align_up(off + sizeof(float) * (size_t)L->KS2 * L->R * Hd);
+  L->err = off;   off = align_up(off + sizeof(int32_t));
   L->total = off;
   return true;
+}
+
+// fp32 -> bf16 hi + bf16 lo with hi + lo == x to ~2^-16 relative.
+__device__ __forceinline__ void split_bf16(float x, __nv_bfloat16* hi, __nv_bfloat16* lo) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  *hi = h;
+  *lo = __float2bfloat16_rn(x - __bfloat162float(h));
 }
 
 __device__ __forceinline__ float block_sum(float x, float* red /* [kThreads/32] */) {
@@ -77,11 +78,11 @@ __device__ __forceinline__ float block_sum(float x, float* red /* [kThreads/32] 
   return t;
 }
 
-// 1. input RMSNorm, one CTA per row.
-__global__ void __launch_bounds__(kThreads) rmsnorm_kernel(const float* __restrict__ hidden,
-                                                           const float* __restrict__ gamma,
-                                                           float* __restrict__ xhat, int Hd,
-                                                           float eps) {
+// 1. input RMSNorm, one CTA per row, written as bf16 hi/lo halves.
+__global__ void __launch_bounds__(kThreads) rmsnorm_split_kernel(const float* __restrict__ hidden,
+                                                                 const float* __restrict__ gamma,
+                                                                 __nv_bfloat16* __restrict__ X2,
+                                                                 int R, int Hd, float eps) {
   __shared__ float red[kThreads / 32];
   const float* x = hidden + (size_t)blockIdx.x * Hd;
   float ss = 0.f;
@@ -91,109 +92,57 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_kernel(const float* __restri
   }
   ss = block_sum(ss, red);
   const float inv = rsqrtf(ss / (float)Hd + eps);
-  float* y = xhat + (size_t)blockIdx.x * Hd;
-  for (int i = threadIdx.x * 4; i < Hd; i += kThreads * 4) {
-    const float4 v = *reinterpret_cast<const float4*>(x + i);
-    const float4 g = *reinterpret_cast<const float4*>(gamma + i);
-    *reinterpret_cast<float4*>(y + i) =
-        make_float4(v.x * inv * g.x, v.y * inv * g.y, v.z * inv * g.z, v.w * inv * g.w);
-  }
+  __nv_bfloat16* hi = X2 + (size_t)blockIdx.x * Hd;
+  __nv_bfloat16* lo = X2 + ((size_t)R + blockIdx.x) * Hd;
+  for (int i = threadIdx.x; i < Hd; i += kThreads) split_bf16(x[i] * inv * gamma[i], hi + i, lo + i);
 }
 
-// Accumulate acc[r][0..1] += sum_{i < kGemmKSub} xs[r][i] * W[i][c .. c+1].
-__device__ __forceinline__ void gemm_substep(float (&acc)[kGemmRows][2],
-                                             const float (*xs)[kGemmKSub + 4],
-                                             const kda_bf16* __restrict__ wp, int N) {
-  uint32_t w[kGemmKSub];
-#pragma unroll
-  for (int i = 0; i < kGemmKSub; ++i) w[i] = __ldg(reinterpret_cast<const unsigned int*>(wp + (size_t)i * N));
-#pragma unroll
-  for (int i = 0; i < kGemmKSub; i += 4) {
-#pragma unroll
-    for (int r = 0; r < kGemmRows; ++r) {
-      const float4 x = *reinterpret_cast<const float4*>(&xs[r][i]);
-      acc[r][0] = fmaf(x.x, bf16_lo(w[i + 0]), acc[r][0]);
-      acc[r][1] = fmaf(x.x, bf16_hi(w[i + 0]), acc[r][1]);
-      acc[r][0] = fmaf(x.y, bf16_lo(w[i + 1]), acc[r][0]);
-      acc[r][1] = fmaf(x.y, bf16_hi(w[i + 1]), acc[r][1]);
-      acc[r][0] = fmaf(x.z, bf16_lo(w[i + 2]), acc[r][0]);
-      acc[r][1] = fmaf(x.z, bf16_hi(w[i + 2]), acc[r][1]);
-      acc[r][0] = fmaf(x.w, bf16_lo(w[i + 3]), acc[r][0]);
-      acc[r][1] = fmaf(x.w, bf16_hi(w[i + 3]), acc[r][1]);
-    }
-  }
-}
-
-// 2./5. skinny split-K GEMM: Ypart[ks][r][c] = sum over the ks-th contraction
-// chunk of X[r][i] * W[i][c].  X fp32 [R, ldx], W bf16 [*, N] (N even).
-// Grid: (ceil(N / 512), KS, ceil(R / 32)).
-__global__ void __launch_bounds__(kThreads, 2) skinny_gemm_kernel(
-    const float* __restrict__ X, int R, int ldx, const kda_bf16* __restrict__ W, int N,
-    int kchunk, float* __restrict__ Ypart) {
-  __shared__ __align__(16) float xs[kGemmRows][kGemmKSub + 4];
-  const int c = (blockIdx.x * kThreads + threadIdx.x) * 2;
-  const int ks = blockIdx.y;
-  const int r0 = blockIdx.z * kGemmRows;
-  const int nrows = min(kGemmRows, R - r0);
-  const int kbeg = ks * kchunk;
-  float acc[kGemmRows][2];
-#pragma unroll
-  for (int r = 0; r < kGemmRows; ++r) acc[r][0] = acc[r][1] = 0.f;
-  for (int kk = 0; kk < kchunk; kk += kGemmKSub) {
-    __syncthreads();
-    for (int e = threadIdx.x; e < kGemmRows * kGemmKSub; e += kThreads) {
-      const int r = e / kGemmKSub, i = e % kGemmKSub;
-      xs[r][i] = (r < nrows) ? X[(size_t)(r0 + r) * ldx + kbeg + kk + i] : 0.f;
-    }
-    __syncthreads();
-    if (c < N) gemm_substep(acc, xs, W + (size_t)(kbeg + kk) * N + c, N);
-  }
-  if (c < N) {
-#pragma unroll
-    for (int r = 0; r < kGemmRows; ++r)
-      if (r < nrows)
-        *reinterpret_cast<float2*>(Ypart + ((size_t)ks * R + r0 + r) * N + c) =
-            make_float2(acc[r][0], acc[r][1]);
-  }
-}
-
-// 3. gate latents: gz[r][c] = f_a[r] . W_fb[:, c] for c < CQ and
-// g_a[r] . W_gb[:, c - CQ] after, f_a and g_a summed from the projection's
-// split-K partials.  Grid: ((CQ + CV) / 512, 1, ceil(R / 32)).
-__global__ void __launch_bounds__(kThreads, 2) latent_gemm_kernel(
+// 3. gate latents on the CUDA cores: gz[r][c] = f_a[r] . W_fb[:, c] for
+// c < CQ and g_a[r] . W_gb[:, c - CQ] after, with f_a and g_a summed from the
+// projection's split-K partials.  Grid ((CQ + CV) / 64, ceil(R / 32)), 128
+// threads: thread t owns columns 2 (t % 32) .. + 1 and rows 8 (t / 32) .. + 7.
+__global__ void __launch_bounds__(128) latent_kernel(
     const float* __restrict__ Ppart, int KS1, int R, int I, int off_fa, int off_ga,
     const kda_bf16* __restrict__ W_fb, int CQ, const kda_bf16* __restrict__ W_gb, int CV,
     float* __restrict__ gz) {
-  __shared__ __align__(16) float xs[kGemmRows][kGemmKSub + 4];
-  const int cglob = (blockIdx.x * kThreads + threadIdx.x) * 2;
-  const bool is_fb = blockIdx.x * kGemmCols < CQ;  // CQ is a multiple of 512
+  __shared__ __align__(16) float xs[kLatRows][kHeadDim];
+  const int c0 = blockIdx.x * kLatCols;
+  const bool is_fb = c0 < CQ;  // CQ is a multiple of 64
   const kda_bf16* W = is_fb ? W_fb : W_gb;
   const int N = is_fb ? CQ : CV;
-  const int c = is_fb ? cglob : cglob - CQ;
+  const int cl = (is_fb ? c0 : c0 - CQ) + 2 * (threadIdx.x & 31);
   const int off = is_fb ? off_fa : off_ga;
-  const int r0 = blockIdx.z * kGemmRows;
-  const int nrows = min(kGemmRows, R - r0);
-  float acc[kGemmRows][2];
-#pragma unroll
-  for (int r = 0; r < kGemmRows; ++r) acc[r][0] = acc[r][1] = 0.f;
-  for (int kk = 0; kk < kHeadDim; kk += kGemmKSub) {
-    __syncthreads();
-    for (int e = threadIdx.x; e < kGemmRows * kGemmKSub; e += kThreads) {
-      const int r = e / kGemmKSub, i = e % kGemmKSub;
-      float v = 0.f;
-      if (r < nrows)
-        for (int ks = 0; ks < KS1; ++ks) v += Ppart[((size_t)ks * R + r0 + r) * I + off + kk + i];
-      xs[r][i] = v;
-    }
-    __syncthreads();
-    if (c < N) gemm_substep(acc, xs, W + (size_t)kk * N + c, N);
+  const int r0 = blockIdx.y * kLatRows;
+  const int rg = threadIdx.x >> 5;
+  for (int e = threadIdx.x; e < kLatRows * kHeadDim; e += 128) {
+    const int r = e / kHeadDim, i = e % kHeadDim;
+    float v = 0.f;
+    if (r0 + r < R)
+      for (int ks = 0; ks < KS1; ++ks) v += Ppart[((size_t)ks * R + r0 + r) * I + off + i];
+    xs[r][i] = v;
   }
-  if (c < N) {
+  __syncthreads();
+  float acc[8][2];
 #pragma unroll
-    for (int r = 0; r < kGemmRows; ++r)
-      if (r < nrows)
-        *reinterpret_cast<float2*>(gz + (size_t)(r0 + r) * (CQ + CV) + cglob) =
-            make_float2(acc[r][0], acc[r][1]);
+  for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = 0.f;
+  const kda_bf16* wp = W + cl;
+#pragma unroll 4
+  for (int k = 0; k < kHeadDim; ++k) {
+    const uint32_t w2 = __ldg(reinterpret_cast<const unsigned int*>(wp + (size_t)k * N));
+    const float w0 = bf16_lo(w2), w1 = bf16_hi(w2);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float xv = xs[rg * 8 + j][k];
+      acc[j][0] = fmaf(xv, w0, acc[j][0]);
+      acc[j][1] = fmaf(xv, w1, acc[j][1]);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int r = r0 + rg * 8 + j;
+    if (r < R)
+      *reinterpret_cast<float2*>(gz + (size_t)r * (CQ + CV) + c0 + 2 * (threadIdx.x & 31)) =
+          make_float2(acc[j][0], acc[j][1]);
   }
 }
 
@@ -206,7 +155,7 @@ struct HeadArgs {
   const float* dt_bias;
   const float* gamma_o;
   float* S;
-  float* on;
+  __nv_bfloat16* on2;  // [2R, CV] bf16 hi rows then lo rows
   float scale, lower_bound, rms_norm_eps, l2_eps;
   int R, I, KS1, nh, Kc, CQ, CV;
 };
@@ -306,7 +255,9 @@ __global__ void __launch_bounds__(kThreads, 2) block_head_kernel(const HeadArgs 
     const int d = tid;
     const float inv = rsqrtf(m2 / (float)kHeadDim + p.rms_norm_eps);
     const float z = p.gz[(size_t)r * (p.CQ + p.CV) + p.CQ + d * p.nh + h];  // W_gb channel-outer
-    p.on[(size_t)r * p.CV + h * kHeadDim + d] = od * inv * p.gamma_o[d] * sigmoidf_(z);
+    const size_t col = (size_t)h * kHeadDim + d;  // W_o rows are head-outer
+    split_bf16(od * inv * p.gamma_o[d] * sigmoidf_(z), p.on2 + (size_t)r * p.CV + col,
+               p.on2 + ((size_t)p.R + r) * p.CV + col);
   }
 }
 
@@ -336,19 +287,22 @@ cudaError_t launch_kda_block(const BlockArgs& a, cudaStream_t stream) {
   Layout L;
   if (!make_layout(a.B, a.n, a.Hd, a.nh, a.K, a.V, a.Kc, &L)) return cudaErrorInvalidValue;
   char* ws = static_cast<char*>(a.workspace);
-  float* xhat = reinterpret_cast<float*>(ws + L.xhat);
+  __nv_bfloat16* x2 = reinterpret_cast<__nv_bfloat16*>(ws + L.x2);
   float* ppart = reinterpret_cast<float*>(ws + L.ppart);
   float* gz = reinterpret_cast<float*>(ws + L.gz);
-  float* on = reinterpret_cast<float*>(ws + L.on);
+  __nv_bfloat16* on2 = reinterpret_cast<__nv_bfloat16*>(ws + L.on2);
   float* opart = reinterpret_cast<float*>(ws + L.opart);
-  const int rblocks = (L.R + kGemmRows - 1) / kGemmRows;
+  int32_t* err = a.dev_status ? a.dev_status : reinterpret_cast<int32_t*>(ws + L.err);
+  cudaError_t e;
 
-  rmsnorm_kernel<<<L.R, kThreads, 0, stream>>>(a.hidden, a.gamma_in, xhat, a.Hd, a.rms_norm_eps);
-  skinny_gemm_kernel<<<dim3((L.I + kGemmCols - 1) / kGemmCols, L.KS1, rblocks), kThreads, 0, stream>>>(
-      xhat, L.R, a.Hd, a.W_in, L.I, L.kchunk1, ppart);
+  rmsnorm_split_kernel<<<L.R, kThreads, 0, stream>>>(a.hidden, a.gamma_in, x2, L.R, a.Hd,
+                                                      a.rms_norm_eps);
+  e = launch_tc_gemm(reinterpret_cast<const kda_bf16*>(x2), L.R, a.Hd, a.W_in, L.I, L.KS1, ppart,
+                     err, stream);
+  if (e != cudaSuccess) return e;
   const int off_ga = 2 * L.CQ + L.CV;
   const int off_fa = off_ga + kHeadDim + a.nh;
-  latent_gemm_kernel<<<dim3((L.CQ + L.CV) / kGemmCols, 1, rblocks), kThreads, 0, stream>>>(
+  latent_kernel<<<dim3((L.CQ + L.CV) / kLatCols, (L.R + kLatRows - 1) / kLatRows), 128, 0, stream>>>(
       ppart, L.KS1, L.R, L.I, off_fa, off_ga, a.W_fb, L.CQ, a.W_gb, L.CV, gz);
   HeadArgs h;
   h.Ppart = ppart;
@@ -359,7 +313,7 @@ cudaError_t launch_kda_block(const BlockArgs& a, cudaStream_t stream) {
   h.dt_bias = a.dt_bias;
   h.gamma_o = a.gamma_o;
   h.S = a.S;
-  h.on = on;
+  h.on2 = on2;
   h.scale = a.scale;
   h.lower_bound = a.lower_bound;
   h.rms_norm_eps = a.rms_norm_eps;
@@ -372,8 +326,9 @@ cudaError_t launch_kda_block(const BlockArgs& a, cudaStream_t stream) {
   h.CQ = L.CQ;
   h.CV = L.CV;
   block_head_kernel<<<L.R * a.nh, kThreads, 0, stream>>>(h);
-  skinny_gemm_kernel<<<dim3((a.Hd + kGemmCols - 1) / kGemmCols, L.KS2, rblocks), kThreads, 0, stream>>>(
-      on, L.R, L.CV, a.W_o, a.Hd, L.kchunk2, opart);
+  e = launch_tc_gemm(reinterpret_cast<const kda_bf16*>(on2), L.R, L.CV, a.W_o, a.Hd, L.KS2, opart,
+                     err, stream);
+  if (e != cudaSuccess) return e;
   const size_t count4 = (size_t)L.R * a.Hd / 4;
   const int rblk = (int)((count4 + kThreads - 1) / kThreads);
   reduce_partials_kernel<<<rblk, kThreads, 0, stream>>>(opart, L.KS2, count4, a.out);

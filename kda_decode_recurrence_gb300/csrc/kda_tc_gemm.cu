@@ -1,0 +1,330 @@
+// kda_tc_gemm.cu -- weight-streaming GEMM on the 5th-generation tensor cores
+// (tcgen05 + TMEM, operands staged by TMA) for the fused block's two dense
+// projections (the fused input projection W_in and the output projection W_o
+// of "KDA Block TKG Kernel API Reference").
+//
+//   Ypart[ks][r][n] = sum_{k in split ks} (Xhi[r][k] + Xlo[r][k]) * W[k][n]
+//
+// W is bf16 [Kdim, N] stored contraction-first (row k contiguous over n);
+// X2 is bf16 [2R, Kdim]: rows 0..R-1 hold the bf16 rounding of the fp32
+// activations, rows R..2R-1 the bf16 rounding of the remainder, so the sum of
+// the two products carries ~16 significant bits of the activation instead of
+// 8 (the weights are exactly bf16).  The path is bound by streaming W from
+// HBM; the doubled MMA work is free.
+//
+// Mapping (swap-AB): MMA M = 128 weight columns (A = W^T tile, MN-major in
+// shared memory), MMA N = the hi and lo copies of up to 128 tokens (B = X2
+// tile, K-major), MMA K = 16 per instruction, 64 per pipeline stage.  The
+// accumulator D[128, N] lives in TMEM.  One CTA per (128-column tile,
+// contraction split, 128-token block); 4 warps: warp 0 allocates TMEM and
+// its lane 0 issues the TMA loads, warp 1 lane 0 issues the MMAs, then all
+// four warps drain TMEM (warp w owns TMEM lanes 32w..32w+31) and write the
+// split's partial sums.  Every wait on an mbarrier is bounded by a 1 s
+// timer; on expiry the CTA records an error bit and returns cleanly.
+#include <cuda.h>
+
+#include "kda_common.cuh"
+#include "kda_tc_gemm.h"
+
+namespace kda {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kBK = 64;                  // contraction rows per stage
+constexpr int kTileN = 128;              // weight columns per CTA (MMA M)
+constexpr int kABytes = kBK * kTileN * 2;  // 16 KiB: two 64x64 swizzled boxes
+constexpr int kBoxRows = 32;             // token rows per TMA box of X2
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// Wait until the phase with the given parity has completed; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t addr = smem_u32(bar);
+  const unsigned long long t0 = global_ns();
+  while (true) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+
+// tcgen05 shared-memory matrix descriptor: start address, leading and stride
+// byte offsets (16-byte units), the fixed descriptor version (bit 46) and the
+// 128-byte swizzle mode (2 in bits 61..63).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A
+// MN-major, B K-major, N and M sizes.
+__device__ __forceinline__ uint32_t instr_desc_bf16(int n, int m) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+struct GemmShape {
+  int R;       // tokens
+  int Kdim;    // contraction length (multiple of 64)
+  int N;       // output columns (multiple of 8)
+  int KS;      // contraction splits
+};
+
+// Dynamic shared memory: kStages x (A 16 KiB + B 2*RB*128 B), 1024-aligned,
+// followed by the mbarriers and the TMEM base address word.
+__global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
+    const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+    float* __restrict__ Ypart, const GemmShape sh, int32_t* __restrict__ err) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * kTileN;
+  const int ks = blockIdx.y;
+  const int r0 = blockIdx.z * 128;
+  const int rows = min(128, sh.R - r0);
+  const int RB = (rows + 31) & ~31;        // token rows per hi/lo half (32..128)
+  const int NM = 2 * RB;                   // MMA N
+  const uint32_t tmem_cols = NM <= 64 ? 64 : (NM <= 128 ? 128 : 256);
+  const int b_bytes = NM * 128;            // hi and lo boxes, 128 B per token row
+  const int stage_bytes = kABytes + b_bytes;
+  const int nkb = sh.Kdim / kBK;
+  const int kb0 = (int)((long long)ks * nkb / sh.KS);
+  const int kb1 = (int)((long long)(ks + 1) * nkb / sh.KS);
+
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * stage_bytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* done = empty + kStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  bool ok = true;
+  if (warp == 0 && lane == 0) {
+    // TMA producer
+    for (int kb = kb0; kb < kb1 && ok; ++kb) {
+      const int i = kb - kb0, s = i % kStages, round = i / kStages;
+      if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1)) { ok = false; break; }
+      unsigned char* a_s = smem + s * stage_bytes;
+      unsigned char* b_s = a_s + kABytes;
+      mbar_expect_tx(&full[s], stage_bytes);
+      const int k0 = kb * kBK;
+      tma_load_2d(a_s, &tmW, &full[s], n0, k0);
+      tma_load_2d(a_s + kABytes / 2, &tmW, &full[s], n0 + 64, k0);
+      for (int j = 0; j < RB / kBoxRows; ++j) {
+        tma_load_2d(b_s + j * kBoxRows * 128, &tmX, &full[s], k0, r0 + j * kBoxRows);
+        tma_load_2d(b_s + (RB + j * kBoxRows) * 128, &tmX, &full[s], k0, sh.R + r0 + j * kBoxRows);
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // MMA issuer
+    const uint32_t idesc = instr_desc_bf16(NM, kTileN);
+    for (int kb = kb0; kb < kb1 && ok; ++kb) {
+      const int i = kb - kb0, s = i % kStages, round = i / kStages;
+      if (!mbar_wait(&full[s], round & 1)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t a_addr = smem_u32(smem + s * stage_bytes);
+      const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+      for (int j = 0; j < kBK / 16; ++j) {
+        // A: MN-major, atoms of 64 columns x 8 rows; next column atom 8 KiB
+        // away (LBO), next 8-row group 1 KiB away (SBO); 16 rows per step.
+        const uint64_t adesc = smem_desc_sw128(a_addr + j * 2048, 8192, 1024);
+        // B: K-major, 128-byte rows, 8-row groups 1 KiB apart; 32 B per step.
+        const uint64_t bdesc = smem_desc_sw128(b_addr + j * 32, 16, 1024);
+        mma_bf16(tmem, adesc, bdesc, idesc, (kb > kb0 || j > 0) ? 1u : 0u);
+      }
+      mma_commit(&empty[s]);
+    }
+    mma_commit(done);
+  }
+  __syncwarp();
+
+  // Epilogue: all four warps.  tcgen05.ld is warp-collective, so a warp
+  // reads TMEM only if all of its lanes saw the accumulator complete.
+  const bool have = __all_sync(0xffffffffu, mbar_wait(done, 0)) != 0;
+  if (!have || !ok) {
+    if (lane == 0) atomicOr(err, 1);
+  }
+  tc_fence_after();
+  const int m = n0 + warp * 32 + lane;
+  if (have) {
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    for (int c = 0; c < RB / 32; ++c) {
+      float hi[32], lo[32];
+      tmem_ld_32cols(lane_base + c * 32, hi);
+      tmem_ld_32cols(lane_base + RB + c * 32, lo);
+      tmem_ld_wait();
+      if (m < sh.N) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int r = r0 + c * 32 + j;
+          if (r < sh.R) Ypart[((size_t)ks * sh.R + r) * sh.N + m] = hi[j] + lo[j];
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(tmem_cols)
+                 : "memory");
+  }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor map: inner extent `inner` (contiguous), outer extent
+// `outer`, box 64 x box_rows, 128-byte swizzle, out-of-range reads as zero.
+bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+              uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+size_t tc_gemm_smem_bytes(int R) {
+  const int rows = R < 128 ? R : 128;
+  const int RB = (rows + 31) & ~31;
+  return 1024 + (size_t)kStages * (kABytes + 2 * RB * 128) + (2 * kStages + 1) * 8 + 16;
+}
+
+cudaError_t launch_tc_gemm(const kda_bf16* X2, int R, int Kdim, const kda_bf16* W, int N, int KS,
+                           float* Ypart, int32_t* err, cudaStream_t stream) {
+  if (R < 1 || Kdim % kBK != 0 || N % 8 != 0 || KS < 1 || KS > Kdim / kBK)
+    return cudaErrorInvalidValue;
+  CUtensorMap tmW, tmX;
+  if (!make_map(&tmW, W, (uint64_t)N, (uint64_t)Kdim, kBK)) return cudaErrorInvalidValue;
+  if (!make_map(&tmX, X2, (uint64_t)Kdim, (uint64_t)2 * R, kBoxRows)) return cudaErrorInvalidValue;
+  const size_t smem = tc_gemm_smem_bytes(R);
+  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  GemmShape sh{R, Kdim, N, KS};
+  dim3 grid((N + kTileN - 1) / kTileN, KS, (R + 127) / 128);
+  tc_gemm_kernel<<<grid, 128, smem, stream>>>(tmW, tmX, Ypart, sh, err);
+  return cudaGetLastError();
+}
+
+}  // namespace kda

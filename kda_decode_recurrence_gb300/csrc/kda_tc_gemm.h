@@ -1,0 +1,22 @@
+// kda_tc_gemm.h -- the tcgen05 weight-streaming GEMM used by the fused block.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+// Ypart[ks][r][n] = sum over contraction split ks of (X2[r][k] + X2[R + r][k]) * W[k][n].
+// X2 bf16 [2R, Kdim] (hi rows then lo rows), W bf16 [Kdim, N] (row k contiguous),
+// Ypart fp32 [KS, R, N].  Kdim % 64 == 0, N % 8 == 0, 1 <= KS <= Kdim / 64,
+// 16-byte aligned pointers.  On an internal pipeline timeout the kernel ORs
+// bit 1 into *err (a device int32) and leaves Ypart incomplete.
+cudaError_t launch_tc_gemm(const kda_bf16* X2, int R, int Kdim, const kda_bf16* W, int N, int KS,
+                           float* Ypart, int32_t* err, cudaStream_t stream);
+
+size_t tc_gemm_smem_bytes(int R);
+
+}  // namespace kda
