@@ -177,6 +177,37 @@ kda_status kda_block_tkg(float* out, const float* hidden, const float* gamma_in,
                          int n, int Hd, int nh, int K, int V, int Kc, void* workspace,
                          size_t workspace_bytes, int32_t* dev_status, void* stream);
 
+/*
+ * kda_block_tkg_static -- kda_block_tkg that allocates nothing and takes no
+ * workspace argument.  The pages have no counterpart to this call: it exists
+ * for callers that cannot hand the block a workspace because their host owns
+ * all device memory (an inference server's memory pool, a plugin interface
+ * that passes a kernel library only its input and output buffers).
+ *
+ * The intermediates live in one fixed 16 MiB device array inside the library
+ * (held on every GPU that loads the library until the process exits), which
+ * serves the Kimi K3 block with B = 32 requests, Hd = 4096, num_head = 32.
+ * Arguments and results are those of kda_block_tkg without workspace and
+ * workspace_bytes.
+ *   - Sizes that need more than 16 MiB of workspace (see
+ *     kda_block_tkg_workspace_size) return KDA_ERR_WORKSPACE before any CUDA
+ *     call.
+ *   - The first call made with a given device current looks up the array's
+ *     device address on that device (cudaGetSymbolAddress) and caches it;
+ *     make that first call before any stream capture.
+ *   - Every call uses the same array and leaves its last contents there, so
+ *     two calls that can run on the GPU at the same time (different streams,
+ *     no ordering between them) race and corrupt each other's results.
+ * No cudaMalloc, cudaFree or other allocating routine is called.
+ */
+kda_status kda_block_tkg_static(float* out, const float* hidden, const float* gamma_in,
+                                const kda_bf16* W_in, const kda_bf16* W_fb, const kda_bf16* W_gb,
+                                const kda_bf16* conv_w, const float* A_log, const float* dt_bias,
+                                const float* gamma_o, const kda_bf16* W_o, float* S,
+                                float* conv_state, float scale, float lower_bound,
+                                float rms_norm_eps, float l2_eps, int B, int n, int Hd, int nh,
+                                int K, int V, int Kc, int32_t* dev_status, void* stream);
+
 /* Bytes of device workspace kda_block_tkg needs for these sizes (0 when the
  * sizes are invalid).  Host-only, no CUDA call. */
 size_t kda_block_tkg_workspace_size(int B, int n, int Hd, int nh, int K, int V, int Kc);

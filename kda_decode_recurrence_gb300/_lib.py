@@ -14,8 +14,8 @@ _lock = threading.Lock()
 _lib = None
 
 # Every symbol include/kda.h declares.
-EXPORTS = ("kda_decode", "kda_block_tkg", "kda_block_tkg_workspace_size", "kda_status_string",
-           "kda_version")
+EXPORTS = ("kda_decode", "kda_block_tkg", "kda_block_tkg_static", "kda_block_tkg_workspace_size",
+           "kda_status_string", "kda_version")
 
 STATUS = {
     0: "KDA_OK", -1: "KDA_ERR_NULL", -2: "KDA_ERR_SHAPE", -3: "KDA_ERR_UNSUPPORTED",
@@ -30,6 +30,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.kda_decode.argtypes = [vp] * 11 + [i, f] + [i] * 7 + [vp, vp]
     lib.kda_block_tkg.restype = i
     lib.kda_block_tkg.argtypes = [vp] * 13 + [f] * 4 + [i] * 7 + [vp, ctypes.c_size_t, vp, vp]
+    lib.kda_block_tkg_static.restype = i
+    lib.kda_block_tkg_static.argtypes = [vp] * 13 + [f] * 4 + [i] * 7 + [vp, vp]
     lib.kda_block_tkg_workspace_size.restype = ctypes.c_size_t
     lib.kda_block_tkg_workspace_size.argtypes = [i] * 7
     lib.kda_status_string.restype = ctypes.c_char_p
