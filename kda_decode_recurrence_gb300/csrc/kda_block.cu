@@ -12,12 +12,16 @@
 //                   (split-K so every SM streams a slice of the 103 MB W_in;
 //                   consumers add the KS1 partial sums)
 //   3. latent       graw = f_a . W_fb, z = g_a . W_gb (CUDA cores)            [R, CQ + CV]
-//   4. head         one CTA per (b, h): short conv + SiLU + conv_state update
-//                   for the head's q, k, v channels, forget gate, beta, L2
-//                   norms, the register-tile delta-rule step on S[b, h] (shared
-//                   with kda_decode), gated output RMSNorm -> bf16 hi/lo on2
-//   5. out GEMM     tcgen05, O_part[ks] = on[:, split ks] . W_o[split ks, :]   [KS2, R, Hd]
-//   6. reduce       out = sum_ks O_part[ks]
+//   4. prep         one CTA per (b, 8 heads), channels read coalesced: short
+//                   conv + SiLU + conv_state update of the q, k, v channels,
+//                   forget gate, beta, L2 norms -> the per-head token vectors
+//                   (the same staging record kda_decode builds) and the output
+//                   gate gamma_o * sigmoid(z)
+//   5. recurrence   one CTA per (b, h): the register-tile delta-rule step on
+//                   S[b, h] (shared with kda_decode), gated output RMSNorm ->
+//                   bf16 hi/lo on2
+//   6. out GEMM     tcgen05, O_part[ks] = on[:, split ks] . W_o[split ks, :]   [KS2, R, Hd]
+//   7. reduce       out = sum_ks O_part[ks]
 // Intermediates live in the caller's workspace (a few MB: L2-resident).
 #include "kda_recurrence.cuh"
 #include "kda_tc_gemm.h"
@@ -33,7 +37,7 @@ constexpr int kKS2 = 8;        // contraction splits of the W_o GEMM
 
 struct Layout {
   int R, I, CQ, CV, KS1, KS2;
-  size_t x2, ppart, gz, on2, opart, err, total;
+  size_t x2, ppart, gz, stage, zgate, on2, opart, err, total;
 };
 
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -52,6 +56,8 @@ bool make_layout(int B, int n, int Hd, int nh, int K, int V, int Kc, Layout* L) 
   L->x2 = off;    off = align_up(off + 2 * sizeof(kda_bf16) * (size_t)L->R * Hd);
   L->ppart = off; off = align_up(off + sizeof(float) * (size_t)L->KS1 * L->R * L->I);
   L->gz = off;    off = align_up(off + sizeof(float) * (size_t)L->R * (L->CQ + L->CV));
+  L->stage = off; off = align_up(off + sizeof(TokenStage) * (size_t)L->R * nh);
+  L->zgate = off; off = align_up(off + sizeof(float) * (size_t)L->R * L->CV);
   L->on2 = off;   off = align_up(off + 2 * sizeof(kda_bf16) * (size_t)L->R * L->CV);
   L->opart = off; off = align_up(off + sizeof(float) * (size_t)L->KS2 * L->R * Hd);
   L->err = off;   off = align_up(off + sizeof(int32_t));
@@ -99,54 +105,70 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_split_kernel(const float* __
 
 // 3. gate latents on the CUDA cores: gz[r][c] = f_a[r] . W_fb[:, c] for
 // c < CQ and g_a[r] . W_gb[:, c - CQ] after, with f_a and g_a summed from the
-// projection's split-K partials.  Grid ((CQ + CV) / 64, ceil(R / 32)), 128
-// threads: thread t owns columns 2 (t % 32) .. + 1 and rows 8 (t / 32) .. + 7.
-__global__ void __launch_bounds__(128) latent_kernel(
+// projection's split-K partials.  Grid ((CQ + CV) / 64, ceil(R / 32)), 256
+// threads.  The CTA first pulls its whole 128 x 64 weight tile and its
+// 32 x 128 activation panel into shared memory with 16-byte loads (one
+// round trip), then thread t computes columns 2 (t % 32) .. + 1 of rows
+// 4 (t / 32) .. + 3.
+__global__ void __launch_bounds__(256) latent_kernel(
     const float* __restrict__ Ppart, int KS1, int R, int I, int off_fa, int off_ga,
     const kda_bf16* __restrict__ W_fb, int CQ, const kda_bf16* __restrict__ W_gb, int CV,
     float* __restrict__ gz) {
   __shared__ __align__(16) float xs[kLatRows][kHeadDim];
+  __shared__ __align__(16) kda_bf16 ws[kHeadDim][kLatCols];
+  const int t = threadIdx.x;
   const int c0 = blockIdx.x * kLatCols;
   const bool is_fb = c0 < CQ;  // CQ is a multiple of 64
   const kda_bf16* W = is_fb ? W_fb : W_gb;
   const int N = is_fb ? CQ : CV;
-  const int cl = (is_fb ? c0 : c0 - CQ) + 2 * (threadIdx.x & 31);
+  const int cbase = is_fb ? c0 : c0 - CQ;
   const int off = is_fb ? off_fa : off_ga;
   const int r0 = blockIdx.y * kLatRows;
-  const int rg = threadIdx.x >> 5;
-  for (int e = threadIdx.x; e < kLatRows * kHeadDim; e += 128) {
-    const int r = e / kHeadDim, i = e % kHeadDim;
-    float v = 0.f;
-    if (r0 + r < R)
-      for (int ks = 0; ks < KS1; ++ks) v += Ppart[((size_t)ks * R + r0 + r) * I + off + i];
-    xs[r][i] = v;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {  // 128 rows x 8 uint4
+    const int e = t + 256 * i, row = e >> 3, q = e & 7;
+    reinterpret_cast<uint4*>(&ws[row][0])[q] =
+        __ldg(reinterpret_cast<const uint4*>(W + (size_t)row * N + cbase) + q);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {  // 32 rows x 32 float4, summed over the splits
+    const int e = t + 256 * i, row = e >> 5, q = e & 31;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r0 + row < R) {
+      for (int ks = 0; ks < KS1; ++ks) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(
+                                   Ppart + ((size_t)ks * R + r0 + row) * I + off) + q);
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      }
+    }
+    reinterpret_cast<float4*>(&xs[row][0])[q] = acc;
   }
   __syncthreads();
-  float acc[8][2];
+  const int cp = t & 31, rq = t >> 5;
+  float acc[4][2];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = 0.f;
-  const kda_bf16* wp = W + cl;
-#pragma unroll 4
+  for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = 0.f;
+#pragma unroll 8
   for (int k = 0; k < kHeadDim; ++k) {
-    const uint32_t w2 = __ldg(reinterpret_cast<const unsigned int*>(wp + (size_t)k * N));
+    const uint32_t w2 = *reinterpret_cast<const uint32_t*>(&ws[k][2 * cp]);
     const float w0 = bf16_lo(w2), w1 = bf16_hi(w2);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float xv = xs[rg * 8 + j][k];
+    for (int j = 0; j < 4; ++j) {
+      const float xv = xs[4 * rq + j][k];
       acc[j][0] = fmaf(xv, w0, acc[j][0]);
       acc[j][1] = fmaf(xv, w1, acc[j][1]);
     }
   }
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int r = r0 + rg * 8 + j;
+  for (int j = 0; j < 4; ++j) {
+    const int r = r0 + 4 * rq + j;
     if (r < R)
-      *reinterpret_cast<float2*>(gz + (size_t)r * (CQ + CV) + c0 + 2 * (threadIdx.x & 31)) =
+      *reinterpret_cast<float2*>(gz + (size_t)r * (CQ + CV) + c0 + 2 * cp) =
           make_float2(acc[j][0], acc[j][1]);
   }
 }
 
-struct HeadArgs {
+struct PrepArgs {
   const float* Ppart;
   const float* gz;
   const kda_bf16* conv_w;
@@ -154,96 +176,136 @@ struct HeadArgs {
   const float* A_log;
   const float* dt_bias;
   const float* gamma_o;
-  float* S;
-  __nv_bfloat16* on2;  // [2R, CV] bf16 hi rows then lo rows
-  float scale, lower_bound, rms_norm_eps, l2_eps;
+  TokenStage* stage;  // [R, nh]
+  float* zgate;       // [R, nh, V]: gamma_o[d] * sigmoid(z)
+  float scale, lower_bound, l2_eps;
   int R, I, KS1, nh, Kc, CQ, CV;
 };
 
-__device__ __forceinline__ float sum_partials(const float* Ppart, int KS1, size_t stride,
-                                              size_t idx) {
-  float v = 0.f;
-  for (int ks = 0; ks < KS1; ++ks) v += Ppart[ks * stride + idx];
-  return v;
-}
-
 // Causal depthwise conv over [conv_state (oldest first), x_new] with taps
 // conv_w[s, 0..Kc-1, c] (tap 0 oldest), SiLU, and the window shift.
-__device__ __forceinline__ float conv_silu_shift(const HeadArgs& p, int b, int s, int c,
+__device__ __forceinline__ float conv_silu_shift(const PrepArgs& p, int b, int s, int c,
                                                  float x_new) {
   const int CS = p.CQ;  // channels per stream (K * nh == V * nh)
   float* cs = p.conv_state + (((size_t)b * 3 + s) * CS + c) * (p.Kc - 1);
-  float win[4];
-  for (int j = 0; j < p.Kc - 1; ++j) win[j] = cs[j];
-  win[p.Kc - 1] = x_new;
+  const unsigned short* w = reinterpret_cast<const unsigned short*>(p.conv_w) + (size_t)s * p.Kc * CS + c;
   float y = 0.f;
-  for (int j = 0; j < p.Kc; ++j) {
-    const unsigned short wb = reinterpret_cast<const unsigned short*>(p.conv_w)[((size_t)s * p.Kc + j) * CS + c];
-    y = fmaf(__uint_as_float((uint32_t)wb << 16), win[j], y);
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    if (j < p.Kc - 1) {
+      const float xj = cs[j];
+      y = fmaf(__uint_as_float((uint32_t)w[(size_t)j * CS] << 16), xj, y);
+      if (j > 0) cs[j - 1] = xj;  // slide the window (cs[j] was read above)
+    }
   }
-  for (int j = 0; j < p.Kc - 1; ++j) cs[j] = win[j + 1];
+  y = fmaf(__uint_as_float((uint32_t)w[(size_t)(p.Kc - 1) * CS] << 16), x_new, y);
+  cs[p.Kc - 2] = x_new;
   return y * sigmoidf_(y);
 }
 
-// 4. one CTA per (request b, head h).
-__global__ void __launch_bounds__(kThreads, 2) block_head_kernel(const HeadArgs p) {
-  __shared__ TokenStage ts;
-  __shared__ float qk_s[2][kHeadDim];
-  __shared__ float o_s[kHeadDim];
-  __shared__ float red[kThreads / 32];
+constexpr int kPrepHeads = 8;
+constexpr int kPrepThreads = kPrepHeads * kHeadDim;  // 1024
 
-  const int h = blockIdx.x % p.nh;
-  const int b = blockIdx.x / p.nh;
-  const int r = b;  // n == 1
+// 4. per (request b, group of 8 heads).  q/k channels are channel-outer
+// (d * nh + h): thread t takes channel (t / 8) * nh + h0 + t % 8, so a warp
+// reads 4 runs of 8 consecutive channels.  v channels and everything per
+// (head, d) use hl = t / 128, d = t % 128 (v is head-outer, so contiguous).
+__global__ void __launch_bounds__(kPrepThreads, 1) block_prep_kernel(const PrepArgs p) {
+  __shared__ float qs_[kPrepHeads][kHeadDim];
+  __shared__ float ks_[kPrepHeads][kHeadDim];
+  __shared__ float red[3][kPrepThreads / 32];
+  const int h0 = blockIdx.x * kPrepHeads;
+  const int r = blockIdx.y;
+  const int b = r;  // n == 1
+  const int t = threadIdx.x;
+  const int dq = t / kPrepHeads, hq = t % kPrepHeads;
+  const int cq = dq * p.nh + h0 + hq;
+  const int hl = t / kHeadDim, d = t % kHeadDim;
+  const int h = h0 + hl;
+  const int cv = h * kHeadDim + d;
+  const size_t pstride = (size_t)p.R * p.I;
+  const float* prow = p.Ppart + (size_t)r * p.I;
+  const int off_beta = 2 * p.CQ + p.CV + kHeadDim;
+
+  float xq = 0.f, xk = 0.f, xv = 0.f, bl = 0.f;
+  for (int ks = 0; ks < p.KS1; ++ks) {
+    const float* pr = prow + ks * pstride;
+    xq += pr[cq];
+    xk += pr[p.CQ + cq];
+    xv += pr[2 * p.CQ + cv];
+    bl += pr[off_beta + h];
+  }
+  const size_t gzrow = (size_t)r * (p.CQ + p.CV);
+  const float graw = p.gz[gzrow + (size_t)h * kHeadDim + d];      // W_fb head-outer
+  const float zz = p.gz[gzrow + p.CQ + (size_t)d * p.nh + h];     // W_gb channel-outer
+  const float dtb = p.dt_bias[(size_t)d * p.nh + h];
+  const float aexp = expf(p.A_log[h]);
+  const float gam = p.gamma_o[d];
+
+  qs_[hq][dq] = conv_silu_shift(p, b, 0, cq, xq);
+  ks_[hq][dq] = conv_silu_shift(p, b, 1, cq, xk);
+  const float yv = conv_silu_shift(p, b, 2, cv, xv);
+  __syncthreads();
+  const float qv = qs_[hl][d], kv = ks_[hl][d];
+  const float qq = warp_sum(qv * qv), kk = warp_sum(kv * kv), qk = warp_sum(qv * kv);
+  const int w = t >> 5;
+  if ((t & 31) == 0) {
+    red[0][w] = qq;
+    red[1][w] = kk;
+    red[2][w] = qk;
+  }
+  __syncthreads();
+  const int w0 = hl * (kHeadDim / 32);  // the 4 warps of head hl
+  float sq = 0.f, sk = 0.f, sqk = 0.f;
+#pragma unroll
+  for (int i = 0; i < kHeadDim / 32; ++i) {
+    sq += red[0][w0 + i];
+    sk += red[1][w0 + i];
+    sqk += red[2][w0 + i];
+  }
+  const float qsc = p.scale * rsqrtf(sq + p.l2_eps);
+  const float ksc = rsqrtf(sk + p.l2_eps);
+  const float beta = sigmoidf_(bl);
+  const float g = p.lower_bound * sigmoidf_(aexp * (graw + dtb));
+  TokenStage& st = p.stage[(size_t)r * p.nh + h];
+  const float kh = kv * ksc;
+  st.row[d] = RowCoef{expf(g), kh, qv * qsc, beta * kh};
+  st.v[d] = yv;
+  if (d == 0) st.bqk = beta * sqk * qsc * ksc;
+  p.zgate[((size_t)r * p.nh + h) * kHeadDim + d] = gam * sigmoidf_(zz);
+}
+
+struct RecArgs {
+  const TokenStage* stage;
+  const float* zgate;
+  float* S;
+  __nv_bfloat16* on2;  // [2R, CV] bf16 hi rows then lo rows
+  float rms_norm_eps;
+  int R, nh, CV;
+};
+
+// 5. one CTA per (request b, head h): the state tile and the staged token
+// vectors are fetched together, one delta-rule step, then the gated output
+// RMSNorm written as bf16 hi/lo for the output projection.
+__global__ void __launch_bounds__(kThreads, 2) block_recurrence_kernel(const RecArgs p) {
+  __shared__ TokenStage ts;
+  __shared__ __align__(16) float zg[kHeadDim];
+  __shared__ __align__(16) float o_s[kHeadDim];
+  __shared__ float red[kThreads / 32];
+  const int bh = blockIdx.x;
+  const int b = bh / p.nh, h = bh - b * p.nh;
   const int tid = threadIdx.x;
   const TileLane tl = tile_lane();
 
-  float* tile = p.S + ((size_t)b * p.nh + h) * (size_t)(kHeadDim * kHeadDim);
+  float* tile = p.S + (size_t)bh * (size_t)(kHeadDim * kHeadDim);
   float4 s[16];
   tile_load(s, tile, tl);
-
-  const size_t pstride = (size_t)p.R * p.I;
-  const float* prow = p.Ppart + (size_t)r * p.I;
-  // q (threads 0..127) and k (128..255): channel-outer d * nh + h
-  {
-    const int sidx = tid >> 7, d = tid & 127;
-    const int c = d * p.nh + h;
-    const float x = sum_partials(prow, p.KS1, pstride, (size_t)sidx * p.CQ + c);
-    qk_s[sidx][d] = conv_silu_shift(p, b, sidx, c, x);
-  }
-  float vval = 0.f;
-  if (tid < kHeadDim) {  // v: head-outer h * V + d
-    const int c = h * kHeadDim + tid;
-    const float x = sum_partials(prow, p.KS1, pstride, (size_t)2 * p.CQ + c);
-    vval = conv_silu_shift(p, b, 2, c, x);
-  }
-  const float beta = sigmoidf_(sum_partials(prow, p.KS1, pstride, (size_t)2 * p.CQ + p.CV + kHeadDim + h));
-  __syncthreads();
-  float qq = 0.f, kk = 0.f, qk = 0.f;
-  if (tid < kHeadDim) {
-    const float qv = qk_s[0][tid], kv = qk_s[1][tid];
-    qq = qv * qv;
-    kk = kv * kv;
-    qk = qv * kv;
-  }
-  qq = block_sum(qq, red);
-  kk = block_sum(kk, red);
-  qk = block_sum(qk, red);
-  const float qs = p.scale * rsqrtf(qq + p.l2_eps);
-  const float ksc = rsqrtf(kk + p.l2_eps);
-  if (tid < kHeadDim) {
-    const int d = tid;
-    const float graw = p.gz[(size_t)r * (p.CQ + p.CV) + h * kHeadDim + d];  // W_fb head-outer
-    const float g = p.lower_bound * sigmoidf_(expf(p.A_log[h]) * (graw + p.dt_bias[(size_t)d * p.nh + h]));
-    RowCoef rc;
-    rc.decay = expf(g);
-    rc.kh = qk_s[1][d] * ksc;
-    rc.qh = qk_s[0][d] * qs;
-    rc.bkh = beta * rc.kh;
-    ts.row[d] = rc;
-    ts.v[d] = vval;
-    if (d == 0) ts.bqk = beta * qk * qs * ksc;
-  }
+  constexpr int kStageVec = (int)(sizeof(TokenStage) / sizeof(uint4));
+  const uint4* src = reinterpret_cast<const uint4*>(p.stage + bh);
+  for (int i = tid; i < kStageVec; i += kThreads) reinterpret_cast<uint4*>(&ts)[i] = src[i];
+  if (tid < kHeadDim / 4)
+    reinterpret_cast<uint4*>(zg)[tid] =
+        reinterpret_cast<const uint4*>(p.zgate + (size_t)bh * kHeadDim)[tid];
   __syncthreads();
   const float4 o = tile_token_step(s, ts, tl);
   if (tl.rg == 0) *reinterpret_cast<float4*>(&o_s[tl.col]) = o;
@@ -252,16 +314,14 @@ __global__ void __launch_bounds__(kThreads, 2) block_head_kernel(const HeadArgs 
   const float od = tid < kHeadDim ? o_s[tid] : 0.f;
   const float m2 = block_sum(od * od, red);
   if (tid < kHeadDim) {
-    const int d = tid;
     const float inv = rsqrtf(m2 / (float)kHeadDim + p.rms_norm_eps);
-    const float z = p.gz[(size_t)r * (p.CQ + p.CV) + p.CQ + d * p.nh + h];  // W_gb channel-outer
-    const size_t col = (size_t)h * kHeadDim + d;  // W_o rows are head-outer
-    split_bf16(od * inv * p.gamma_o[d] * sigmoidf_(z), p.on2 + (size_t)r * p.CV + col,
-               p.on2 + ((size_t)p.R + r) * p.CV + col);
+    const size_t col = (size_t)h * kHeadDim + tid;  // W_o rows are head-outer
+    split_bf16(od * inv * zg[tid], p.on2 + (size_t)b * p.CV + col,
+               p.on2 + ((size_t)p.R + b) * p.CV + col);
   }
 }
 
-// 6. out = sum of the split-K partials (float4 granularity).
+// 7. out = sum of the split-K partials (float4 granularity).
 __global__ void reduce_partials_kernel(const float* __restrict__ part, int KS, size_t count4,
                                        float* __restrict__ out) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < count4;
@@ -302,30 +362,41 @@ cudaError_t launch_kda_block(const BlockArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int off_ga = 2 * L.CQ + L.CV;
   const int off_fa = off_ga + kHeadDim + a.nh;
-  latent_kernel<<<dim3((L.CQ + L.CV) / kLatCols, (L.R + kLatRows - 1) / kLatRows), 128, 0, stream>>>(
+  latent_kernel<<<dim3((L.CQ + L.CV) / kLatCols, (L.R + kLatRows - 1) / kLatRows), 256, 0, stream>>>(
       ppart, L.KS1, L.R, L.I, off_fa, off_ga, a.W_fb, L.CQ, a.W_gb, L.CV, gz);
-  HeadArgs h;
-  h.Ppart = ppart;
-  h.gz = gz;
-  h.conv_w = a.conv_w;
-  h.conv_state = a.conv_state;
-  h.A_log = a.A_log;
-  h.dt_bias = a.dt_bias;
-  h.gamma_o = a.gamma_o;
-  h.S = a.S;
-  h.on2 = on2;
-  h.scale = a.scale;
-  h.lower_bound = a.lower_bound;
-  h.rms_norm_eps = a.rms_norm_eps;
-  h.l2_eps = a.l2_eps;
-  h.R = L.R;
-  h.I = L.I;
-  h.KS1 = L.KS1;
-  h.nh = a.nh;
-  h.Kc = a.Kc;
-  h.CQ = L.CQ;
-  h.CV = L.CV;
-  block_head_kernel<<<L.R * a.nh, kThreads, 0, stream>>>(h);
+  TokenStage* stage = reinterpret_cast<TokenStage*>(ws + L.stage);
+  float* zgate = reinterpret_cast<float*>(ws + L.zgate);
+  PrepArgs pa;
+  pa.Ppart = ppart;
+  pa.gz = gz;
+  pa.conv_w = a.conv_w;
+  pa.conv_state = a.conv_state;
+  pa.A_log = a.A_log;
+  pa.dt_bias = a.dt_bias;
+  pa.gamma_o = a.gamma_o;
+  pa.stage = stage;
+  pa.zgate = zgate;
+  pa.scale = a.scale;
+  pa.lower_bound = a.lower_bound;
+  pa.l2_eps = a.l2_eps;
+  pa.R = L.R;
+  pa.I = L.I;
+  pa.KS1 = L.KS1;
+  pa.nh = a.nh;
+  pa.Kc = a.Kc;
+  pa.CQ = L.CQ;
+  pa.CV = L.CV;
+  block_prep_kernel<<<dim3(a.nh / kPrepHeads, L.R), kPrepThreads, 0, stream>>>(pa);
+  RecArgs ra;
+  ra.stage = stage;
+  ra.zgate = zgate;
+  ra.S = a.S;
+  ra.on2 = on2;
+  ra.rms_norm_eps = a.rms_norm_eps;
+  ra.R = L.R;
+  ra.nh = a.nh;
+  ra.CV = L.CV;
+  block_recurrence_kernel<<<L.R * a.nh, kThreads, 0, stream>>>(ra);
   e = launch_tc_gemm(reinterpret_cast<const kda_bf16*>(on2), L.R, L.CV, a.W_o, a.Hd, L.KS2, opart,
                      err, stream);
   if (e != cudaSuccess) return e;
