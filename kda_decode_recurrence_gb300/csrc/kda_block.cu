@@ -24,6 +24,7 @@
 //   7. reduce       out = sum_ks O_part[ks]
 // Intermediates live in the caller's workspace (a few MB: L2-resident).
 #include "kda_recurrence.cuh"
+#include "kda_launch.h"
 #include "kda_tc_gemm.h"
 
 namespace kda {
@@ -90,6 +91,7 @@ __global__ void __launch_bounds__(kThreads) rmsnorm_split_kernel(const float* __
                                                                  __nv_bfloat16* __restrict__ X2,
                                                                  int R, int Hd, float eps) {
   __shared__ float red[kThreads / 32];
+  pdl_trigger();
   const float* x = hidden + (size_t)blockIdx.x * Hd;
   float ss = 0.f;
   for (int i = threadIdx.x * 4; i < Hd; i += kThreads * 4) {
@@ -130,6 +132,8 @@ __global__ void __launch_bounds__(256) latent_kernel(
     reinterpret_cast<uint4*>(&ws[row][0])[q] =
         __ldg(reinterpret_cast<const uint4*>(W + (size_t)row * N + cbase) + q);
   }
+  pdl_wait();  // the partial sums come from the projection GEMM
+  pdl_trigger();
 #pragma unroll
   for (int i = 0; i < 4; ++i) {  // 32 rows x 32 float4, summed over the splits
     const int e = t + 256 * i, row = e >> 5, q = e & 31;
@@ -182,24 +186,39 @@ struct PrepArgs {
   int R, I, KS1, nh, Kc, CQ, CV;
 };
 
-// Causal depthwise conv over [conv_state (oldest first), x_new] with taps
-// conv_w[s, 0..Kc-1, c] (tap 0 oldest), SiLU, and the window shift.
-__device__ __forceinline__ float conv_silu_shift(const PrepArgs& p, int b, int s, int c,
-                                                 float x_new) {
+// One channel of the depthwise causal conv: the window is conv_state[b, s, c,
+// 0..Kc-2] (oldest first) followed by the new projection value; taps
+// conv_w[s, 0..Kc-1, c] (tap 0 oldest).
+struct ConvChannel {
+  float* state;  // &conv_state[b, s, c, 0]
+  float win[3];  // previous Kc-1 inputs
+  float tap[4];
+};
+
+__device__ __forceinline__ void conv_fetch(const PrepArgs& p, int b, int s, int c, ConvChannel& ch) {
   const int CS = p.CQ;  // channels per stream (K * nh == V * nh)
-  float* cs = p.conv_state + (((size_t)b * 3 + s) * CS + c) * (p.Kc - 1);
+  ch.state = p.conv_state + (((size_t)b * 3 + s) * CS + c) * (p.Kc - 1);
   const unsigned short* w = reinterpret_cast<const unsigned short*>(p.conv_w) + (size_t)s * p.Kc * CS + c;
+#pragma unroll
+  for (int j = 0; j < 3; ++j) ch.win[j] = (j < p.Kc - 1) ? ch.state[j] : 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    ch.tap[j] = (j < p.Kc) ? __uint_as_float((uint32_t)w[(size_t)j * CS] << 16) : 0.f;
+}
+
+// y = SiLU(sum_j tap[j] * window[j]); the state keeps the last Kc-1 inputs.
+__device__ __forceinline__ float conv_apply(const PrepArgs& p, ConvChannel& ch, float x_new) {
   float y = 0.f;
 #pragma unroll
-  for (int j = 0; j < 3; ++j) {
-    if (j < p.Kc - 1) {
-      const float xj = cs[j];
-      y = fmaf(__uint_as_float((uint32_t)w[(size_t)j * CS] << 16), xj, y);
-      if (j > 0) cs[j - 1] = xj;  // slide the window (cs[j] was read above)
-    }
-  }
-  y = fmaf(__uint_as_float((uint32_t)w[(size_t)(p.Kc - 1) * CS] << 16), x_new, y);
-  cs[p.Kc - 2] = x_new;
+  for (int j = 0; j < 3; ++j)
+    if (j < p.Kc - 1) y = fmaf(ch.tap[j], ch.win[j], y);
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (j == p.Kc - 1) y = fmaf(ch.tap[j], x_new, y);
+#pragma unroll
+  for (int j = 1; j < 3; ++j)
+    if (j < p.Kc - 1) ch.state[j - 1] = ch.win[j];
+  ch.state[p.Kc - 2] = x_new;
   return y * sigmoidf_(y);
 }
 
@@ -227,6 +246,17 @@ __global__ void __launch_bounds__(kPrepThreads, 1) block_prep_kernel(const PrepA
   const float* prow = p.Ppart + (size_t)r * p.I;
   const int off_beta = 2 * p.CQ + p.CV + kHeadDim;
 
+  // Inputs no earlier kernel of this call writes: fetched before waiting.
+  ConvChannel chq, chk, chv;
+  conv_fetch(p, b, 0, cq, chq);
+  conv_fetch(p, b, 1, cq, chk);
+  conv_fetch(p, b, 2, cv, chv);
+  const float dtb = p.dt_bias[(size_t)d * p.nh + h];
+  const float aexp = expf(p.A_log[h]);
+  const float gam = p.gamma_o[d];
+  pdl_wait();
+  pdl_trigger();
+
   float xq = 0.f, xk = 0.f, xv = 0.f, bl = 0.f;
   for (int ks = 0; ks < p.KS1; ++ks) {
     const float* pr = prow + ks * pstride;
@@ -238,13 +268,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1) block_prep_kernel(const PrepA
   const size_t gzrow = (size_t)r * (p.CQ + p.CV);
   const float graw = p.gz[gzrow + (size_t)h * kHeadDim + d];      // W_fb head-outer
   const float zz = p.gz[gzrow + p.CQ + (size_t)d * p.nh + h];     // W_gb channel-outer
-  const float dtb = p.dt_bias[(size_t)d * p.nh + h];
-  const float aexp = expf(p.A_log[h]);
-  const float gam = p.gamma_o[d];
 
-  qs_[hq][dq] = conv_silu_shift(p, b, 0, cq, xq);
-  ks_[hq][dq] = conv_silu_shift(p, b, 1, cq, xk);
-  const float yv = conv_silu_shift(p, b, 2, cv, xv);
+  qs_[hq][dq] = conv_apply(p, chq, xq);
+  ks_[hq][dq] = conv_apply(p, chk, xk);
+  const float yv = conv_apply(p, chv, xv);
   __syncthreads();
   const float qv = qs_[hl][d], kv = ks_[hl][d];
   const float qq = warp_sum(qv * qv), kk = warp_sum(kv * kv), qk = warp_sum(qv * kv);
@@ -299,7 +326,9 @@ __global__ void __launch_bounds__(kThreads, 2) block_recurrence_kernel(const Rec
 
   float* tile = p.S + (size_t)bh * (size_t)(kHeadDim * kHeadDim);
   float4 s[16];
-  tile_load(s, tile, tl);
+  tile_load(s, tile, tl);  // S is not written by the preceding kernels
+  pdl_wait();
+  pdl_trigger();
   constexpr int kStageVec = (int)(sizeof(TokenStage) / sizeof(uint4));
   const uint4* src = reinterpret_cast<const uint4*>(p.stage + bh);
   for (int i = tid; i < kStageVec; i += kThreads) reinterpret_cast<uint4*>(&ts)[i] = src[i];
@@ -324,6 +353,7 @@ __global__ void __launch_bounds__(kThreads, 2) block_recurrence_kernel(const Rec
 // 7. out = sum of the split-K partials (float4 granularity).
 __global__ void reduce_partials_kernel(const float* __restrict__ part, int KS, size_t count4,
                                        float* __restrict__ out) {
+  pdl_wait();
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < count4;
        i += (size_t)gridDim.x * blockDim.x) {
     float4 acc = reinterpret_cast<const float4*>(part)[i];
@@ -355,15 +385,20 @@ cudaError_t launch_kda_block(const BlockArgs& a, cudaStream_t stream) {
   int32_t* err = a.dev_status ? a.dev_status : reinterpret_cast<int32_t*>(ws + L.err);
   cudaError_t e;
 
-  rmsnorm_split_kernel<<<L.R, kThreads, 0, stream>>>(a.hidden, a.gamma_in, x2, L.R, a.Hd,
-                                                      a.rms_norm_eps);
+  // The first kernel waits for everything before it in the stream; each later
+  // kernel is a programmatic dependent of the one before it.
+  e = launch(rmsnorm_split_kernel, dim3(L.R), dim3(kThreads), 0, stream, false, a.hidden,
+             a.gamma_in, x2, L.R, a.Hd, a.rms_norm_eps);
+  if (e != cudaSuccess) return e;
   e = launch_tc_gemm(reinterpret_cast<const kda_bf16*>(x2), L.R, a.Hd, a.W_in, L.I, L.KS1, ppart,
-                     err, stream);
+                     err, stream, true);
   if (e != cudaSuccess) return e;
   const int off_ga = 2 * L.CQ + L.CV;
   const int off_fa = off_ga + kHeadDim + a.nh;
-  latent_kernel<<<dim3((L.CQ + L.CV) / kLatCols, (L.R + kLatRows - 1) / kLatRows), 256, 0, stream>>>(
-      ppart, L.KS1, L.R, L.I, off_fa, off_ga, a.W_fb, L.CQ, a.W_gb, L.CV, gz);
+  e = launch(latent_kernel, dim3((L.CQ + L.CV) / kLatCols, (L.R + kLatRows - 1) / kLatRows),
+             dim3(256), 0, stream, true, (const float*)ppart, L.KS1, L.R, L.I, off_fa, off_ga,
+             a.W_fb, L.CQ, a.W_gb, L.CV, gz);
+  if (e != cudaSuccess) return e;
   TokenStage* stage = reinterpret_cast<TokenStage*>(ws + L.stage);
   float* zgate = reinterpret_cast<float*>(ws + L.zgate);
   PrepArgs pa;
@@ -386,7 +421,9 @@ cudaError_t launch_kda_block(const BlockArgs& a, cudaStream_t stream) {
   pa.Kc = a.Kc;
   pa.CQ = L.CQ;
   pa.CV = L.CV;
-  block_prep_kernel<<<dim3(a.nh / kPrepHeads, L.R), kPrepThreads, 0, stream>>>(pa);
+  e = launch(block_prep_kernel, dim3(a.nh / kPrepHeads, L.R), dim3(kPrepThreads), 0, stream, true,
+             pa);
+  if (e != cudaSuccess) return e;
   RecArgs ra;
   ra.stage = stage;
   ra.zgate = zgate;
@@ -396,14 +433,15 @@ cudaError_t launch_kda_block(const BlockArgs& a, cudaStream_t stream) {
   ra.R = L.R;
   ra.nh = a.nh;
   ra.CV = L.CV;
-  block_recurrence_kernel<<<L.R * a.nh, kThreads, 0, stream>>>(ra);
+  e = launch(block_recurrence_kernel, dim3(L.R * a.nh), dim3(kThreads), 0, stream, true, ra);
+  if (e != cudaSuccess) return e;
   e = launch_tc_gemm(reinterpret_cast<const kda_bf16*>(on2), L.R, L.CV, a.W_o, a.Hd, L.KS2, opart,
-                     err, stream);
+                     err, stream, true);
   if (e != cudaSuccess) return e;
   const size_t count4 = (size_t)L.R * a.Hd / 4;
   const int rblk = (int)((count4 + kThreads - 1) / kThreads);
-  reduce_partials_kernel<<<rblk, kThreads, 0, stream>>>(opart, L.KS2, count4, a.out);
-  return cudaGetLastError();
+  return launch(reduce_partials_kernel, dim3(rblk), dim3(kThreads), 0, stream, true,
+                (const float*)opart, L.KS2, count4, a.out);
 }
 
 }  // namespace kda

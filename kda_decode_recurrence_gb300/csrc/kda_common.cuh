@@ -27,6 +27,16 @@ __device__ __forceinline__ float sigmoidf_(float x) { return __frcp_rn(1.0f + ex
 // log(1 + e^x) without overflow: max(x, 0) + log1p(e^-|x|).
 __device__ __forceinline__ float softplusf_(float x) { return fmaxf(x, 0.0f) + log1pf(expf(-fabsf(x))); }
 
+// Programmatic dependent launch.  pdl_wait() returns once the preceding grid
+// in the stream has completed and its writes are visible (a no-op when this
+// grid was launched normally); pdl_trigger() lets the next grid be scheduled
+// before this one finishes.  A kernel may read inputs that no earlier kernel
+// of the same call writes before pdl_wait(), and writes nothing before it.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void raise_status(int32_t* status, int32_t bit) {
   if (status != nullptr) atomicOr(status, bit);
 }

@@ -24,6 +24,7 @@
 #include <cuda.h>
 
 #include "kda_common.cuh"
+#include "kda_launch.h"
 #include "kda_tc_gemm.h"
 
 namespace kda {
@@ -194,18 +195,34 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // The weights do not depend on the preceding kernel: the first stages'
+  // weight tiles are requested before waiting for it.
+  const int pre = min(kStages, kb1 - kb0);
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < pre; ++i) {
+      unsigned char* a_s = smem + i * stage_bytes;
+      mbar_expect_tx(&full[i], stage_bytes);
+      tma_load_2d(a_s, &tmW, &full[i], n0, (kb0 + i) * kBK);
+      tma_load_2d(a_s + kABytes / 2, &tmW, &full[i], n0 + 64, (kb0 + i) * kBK);
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
+
   bool ok = true;
   if (warp == 0 && lane == 0) {
     // TMA producer
     for (int kb = kb0; kb < kb1 && ok; ++kb) {
       const int i = kb - kb0, s = i % kStages, round = i / kStages;
-      if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1)) { ok = false; break; }
       unsigned char* a_s = smem + s * stage_bytes;
       unsigned char* b_s = a_s + kABytes;
-      mbar_expect_tx(&full[s], stage_bytes);
       const int k0 = kb * kBK;
-      tma_load_2d(a_s, &tmW, &full[s], n0, k0);
-      tma_load_2d(a_s + kABytes / 2, &tmW, &full[s], n0 + 64, k0);
+      if (i >= pre) {
+        if (!mbar_wait(&empty[s], (round - 1) & 1)) { ok = false; break; }
+        mbar_expect_tx(&full[s], stage_bytes);
+        tma_load_2d(a_s, &tmW, &full[s], n0, k0);
+        tma_load_2d(a_s + kABytes / 2, &tmW, &full[s], n0 + 64, k0);
+      }
       for (int j = 0; j < RB / kBoxRows; ++j) {
         tma_load_2d(b_s + j * kBoxRows * 128, &tmX, &full[s], k0, r0 + j * kBoxRows);
         tma_load_2d(b_s + (RB + j * kBoxRows) * 128, &tmX, &full[s], k0, sh.R + r0 + j * kBoxRows);
@@ -311,7 +328,7 @@ size_t tc_gemm_smem_bytes(int R) {
 }
 
 cudaError_t launch_tc_gemm(const kda_bf16* X2, int R, int Kdim, const kda_bf16* W, int N, int KS,
-                           float* Ypart, int32_t* err, cudaStream_t stream) {
+                           float* Ypart, int32_t* err, cudaStream_t stream, bool pdl) {
   if (R < 1 || Kdim % kBK != 0 || N % 8 != 0 || KS < 1 || KS > Kdim / kBK)
     return cudaErrorInvalidValue;
   CUtensorMap tmW, tmX;
@@ -323,8 +340,7 @@ cudaError_t launch_tc_gemm(const kda_bf16* X2, int R, int Kdim, const kda_bf16* 
   if (e != cudaSuccess) return e;
   GemmShape sh{R, Kdim, N, KS};
   dim3 grid((N + kTileN - 1) / kTileN, KS, (R + 127) / 128);
-  tc_gemm_kernel<<<grid, 128, smem, stream>>>(tmW, tmX, Ypart, sh, err);
-  return cudaGetLastError();
+  return launch(tc_gemm_kernel, grid, dim3(128), smem, stream, pdl, tmW, tmX, Ypart, sh, err);
 }
 
 }  // namespace kda

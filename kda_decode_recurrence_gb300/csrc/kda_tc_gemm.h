@@ -13,9 +13,11 @@ namespace kda {
 // X2 bf16 [2R, Kdim] (hi rows then lo rows), W bf16 [Kdim, N] (row k contiguous),
 // Ypart fp32 [KS, R, N].  Kdim % 64 == 0, N % 8 == 0, 1 <= KS <= Kdim / 64,
 // 16-byte aligned pointers.  On an internal pipeline timeout the kernel ORs
-// bit 1 into *err (a device int32) and leaves Ypart incomplete.
+// bit 1 into *err (a device int32) and leaves Ypart incomplete.  With `pdl`
+// the kernel is a programmatic dependent of the previous kernel in the stream
+// (it requests its first weight tiles before waiting for that kernel).
 cudaError_t launch_tc_gemm(const kda_bf16* X2, int R, int Kdim, const kda_bf16* W, int N, int KS,
-                           float* Ypart, int32_t* err, cudaStream_t stream);
+                           float* Ypart, int32_t* err, cudaStream_t stream, bool pdl);
 
 size_t tc_gemm_smem_bytes(int R);
 
