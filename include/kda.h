@@ -69,6 +69,8 @@ typedef enum kda_status {
 #define KDA_DEV_BAD_SLOT 1   /* state_indices[b] >= max_slots: request b skipped, rows zeroed */
 #define KDA_DEV_BAD_SEQLEN 2 /* cu_seqlens not 0 <= cu[b] <= cu[b+1] <= T, or cu[0] != 0, or
                                 cu[B] != T: a request with a bad range is skipped              */
+#define KDA_DEV_TIMEOUT 4    /* an internal copy/tensor-core pipeline wait exceeded its 1 s limit;
+                                the kernel stopped early and its results are incomplete          */
 
 /*
  * kda_decode -- advance each request's recurrent state over its new tokens.
@@ -165,8 +167,8 @@ kda_status kda_decode(float* output, const kda_bf16* q, const kda_bf16* k, const
  *   workspace  device scratch of at least kda_block_tkg_workspace_size(...)
  *              bytes, 256-byte aligned; contents need not be initialised and
  *              are clobbered.
- *   dev_status nullable device int32 (no device-detected errors today; kept
- *              for symmetry).
+ *   dev_status nullable device int32; KDA_DEV_TIMEOUT is the only bit the
+ *              block can set.
  * All pointers 16-byte aligned.
  */
 kda_status kda_block_tkg(float* out, const float* hidden, const float* gamma_in,

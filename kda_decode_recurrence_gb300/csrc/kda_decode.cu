@@ -6,46 +6,68 @@
 // the request's tokens by decay -> delta write -> read, and written back.
 //
 // GB300 design (HBM-bound: 64 KiB in + 64 KiB out per tile, ~1 flop/byte):
-//   * one 256-thread CTA per (request, value head) tile; two CTAs per SM so one
-//     tile's loads are in flight while the other computes;
-//   * the tile is loaded once, straight into registers, with 128-bit streaming
-//     loads (each warp instruction covers 8 rows x 64 contiguous bytes), held
-//     on chip across all of the request's tokens, and stored once;
-//   * warp w owns value columns [16w, 16w + 16); lane = (row group rg 0..7,
-//     column quad cg 0..3) and holds rows rg, rg + 8, ..., rg + 120 of its four
-//     columns (16 float4 = 64 registers);
+//   * a persistent grid, one 256-thread CTA per SM; CTA c takes the
+//     (request, value head) work items c, c + G, c + 2G, ... (G = grid size);
+//   * each tile is fetched with one 64 KiB bulk copy (cp.async.bulk, the
+//     non-tensor TMA path) into a 3-deep shared-memory ring, so up to three
+//     tiles per SM are in flight while the CTA computes on the current one;
+//     an mbarrier per ring slot carries the copy's byte count, and every
+//     item arrives on its slot (with zero bytes when it has no tile to
+//     fetch) so the ring's phases advance uniformly;
+//   * the tile moves from shared memory into registers once and stays there
+//     across all of the request's tokens: warp w owns value columns
+//     [16w, 16w + 16); lane = (row group rg 0..7, column quad cg 0..3) holds
+//     rows rg, rg + 8, ..., rg + 120 of its four columns (16 float4);
 //   * the k- and q-contractions over the 128 key rows are in-thread sums over
-//     16 rows followed by three xor-shuffles across the 8 row groups, so warps
-//     never wait for each other inside a token;
-//   * per-token vectors (normalised q and k, exp(g), beta * k, v, beta, q.k)
-//     are prepared once per CTA, one warp per token, in shared memory, up to 8
-//     tokens per staging round.
+//     16 rows followed by three xor-shuffles across the 8 row groups;
+//   * each warp prepares its own copy of the token's vectors (normalised q
+//     and k, exp(g), beta * k, v, beta * q.k) in a private shared-memory
+//     record, so warps never wait for each other inside an item;
+//   * the advanced tile is written back from registers with 128-bit
+//     streaming stores.
 //
 // The read uses q^T S_new = q^T (D S) + beta (q.k) u with u = v - k^T (D S),
 // which is the same quantity as reading after the write, with one pass over
 // the tile per token instead of two.
+#include "kda_async.cuh"
 #include "kda_recurrence.cuh"
 
 namespace kda {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kChunk = 8;  // tokens staged per round (one warp each)
+constexpr int kWarps = kThreads / 32;
+constexpr int kBufs = 3;  // tiles in flight per CTA
+constexpr uint32_t kTileBytes = kHeadDim * kHeadDim * sizeof(float);
 constexpr float kL2Eps = 1e-6f;
 
-__device__ __forceinline__ void stage_token(const DecodeArgs& p, int t, int h, int hv,
-                                            float a_exp, float q_scale, TokenStage& ts,
-                                            int lane) {
-  const int r0 = lane * 4;
-  const uint2 qraw = *reinterpret_cast<const uint2*>(p.q + ((size_t)t * p.H + h) * kHeadDim + r0);
-  const uint2 kraw = *reinterpret_cast<const uint2*>(p.k + ((size_t)t * p.H + h) * kHeadDim + r0);
-  const uint2 vraw = *reinterpret_cast<const uint2*>(p.v + ((size_t)t * p.HV + hv) * kHeadDim + r0);
-  const float4 raw = *reinterpret_cast<const float4*>(p.raw_gate + ((size_t)t * p.HV + hv) * kHeadDim + r0);
-  const float4 bias = *reinterpret_cast<const float4*>(p.dt_bias + (size_t)hv * kHeadDim + r0);
-  const float beta_logit = p.beta_logits[(size_t)t * p.HV + hv];
+// One token's inputs for the 4 key rows (and 4 value columns) a lane stages.
+struct TokenIn {
+  uint2 q, k, v;      // 4 bf16 each
+  float4 raw, bias;   // raw gate and dt_bias
+  float beta_logit, a_log;
+};
 
-  const float q[4] = {bf16_lo(qraw.x), bf16_hi(qraw.x), bf16_lo(qraw.y), bf16_hi(qraw.y)};
-  const float k[4] = {bf16_lo(kraw.x), bf16_hi(kraw.x), bf16_lo(kraw.y), bf16_hi(kraw.y)};
+__device__ __forceinline__ TokenIn fetch_token(const DecodeArgs& p, int t, int h, int hv, int lane) {
+  const int r0 = lane * 4;
+  TokenIn in;
+  in.q = __ldg(reinterpret_cast<const uint2*>(p.q + ((size_t)t * p.H + h) * kHeadDim + r0));
+  in.k = __ldg(reinterpret_cast<const uint2*>(p.k + ((size_t)t * p.H + h) * kHeadDim + r0));
+  in.v = __ldg(reinterpret_cast<const uint2*>(p.v + ((size_t)t * p.HV + hv) * kHeadDim + r0));
+  in.raw = __ldg(reinterpret_cast<const float4*>(p.raw_gate + ((size_t)t * p.HV + hv) * kHeadDim + r0));
+  in.bias = __ldg(reinterpret_cast<const float4*>(p.dt_bias + (size_t)hv * kHeadDim + r0));
+  in.beta_logit = __ldg(p.beta_logits + (size_t)t * p.HV + hv);
+  in.a_log = __ldg(p.a_log + hv);
+  return in;
+}
+
+// Build the warp's token record: L2 norms (warp reductions), the scaled
+// query, the gate and decay exp(g), beta and beta * (qh . kh).
+__device__ __forceinline__ void build_stage(const DecodeArgs& p, const TokenIn& in,
+                                            TokenStage& ts, int lane) {
+  const int r0 = lane * 4;
+  const float q[4] = {bf16_lo(in.q.x), bf16_hi(in.q.x), bf16_lo(in.q.y), bf16_hi(in.q.y)};
+  const float k[4] = {bf16_lo(in.k.x), bf16_hi(in.k.x), bf16_lo(in.k.y), bf16_hi(in.k.y)};
   float qq = 0.f, kk = 0.f, qk = 0.f;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -56,10 +78,12 @@ __device__ __forceinline__ void stage_token(const DecodeArgs& p, int t, int h, i
   qq = warp_sum(qq);
   kk = warp_sum(kk);
   qk = warp_sum(qk);
-  const float qs = q_scale * rsqrtf(qq + kL2Eps);
+  const float qs = p.q_scale * rsqrtf(qq + kL2Eps);
   const float ks = rsqrtf(kk + kL2Eps);
-  const float beta = sigmoidf_(beta_logit);
-  const float xr[4] = {raw.x + bias.x, raw.y + bias.y, raw.z + bias.z, raw.w + bias.w};
+  const float beta = sigmoidf_(in.beta_logit);
+  const float a_exp = expf(in.a_log);
+  const float xr[4] = {in.raw.x + in.bias.x, in.raw.y + in.bias.y, in.raw.z + in.bias.z,
+                       in.raw.w + in.bias.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float g = (p.gate_mode == KDA_GATE_SOFTPLUS) ? -a_exp * softplusf_(xr[i])
@@ -67,74 +91,171 @@ __device__ __forceinline__ void stage_token(const DecodeArgs& p, int t, int h, i
     const float kh = k[i] * ks;
     ts.row[r0 + i] = RowCoef{expf(g), kh, q[i] * qs, beta * kh};
   }
-  ts.v[r0 + 0] = bf16_lo(vraw.x);
-  ts.v[r0 + 1] = bf16_hi(vraw.x);
-  ts.v[r0 + 2] = bf16_lo(vraw.y);
-  ts.v[r0 + 3] = bf16_hi(vraw.y);
+  *reinterpret_cast<float4*>(&ts.v[r0]) =
+      make_float4(bf16_lo(in.v.x), bf16_hi(in.v.x), bf16_lo(in.v.y), bf16_hi(in.v.y));
   if (lane == 0) ts.bqk = beta * qk * qs * ks;
 }
 
-__global__ void __launch_bounds__(kThreads, 2) kda_decode_kernel(const DecodeArgs p) {
-  __shared__ TokenStage stage[kChunk];
+struct Item {
+  int b, hv, slot, t0, t1;
+  bool range_ok;  // 0 <= t0 <= t1 <= T
+  bool slot_ok;   // 0 <= slot < max_slots
+  __device__ __forceinline__ bool has_tile() const { return range_ok && slot_ok && t1 > t0; }
+};
 
-  const int item = blockIdx.x;
-  const int b = item / p.HV;
-  const int hv = item - b * p.HV;
-  const int warp = threadIdx.x >> 5;
+__device__ __forceinline__ Item load_item(const DecodeArgs& p, long long item) {
+  Item d;
+  d.b = (int)(item / p.HV);
+  d.hv = (int)(item - (long long)d.b * p.HV);
+  d.slot = __ldg(p.state_indices + d.b);
+  d.t0 = __ldg(p.cu_seqlens + d.b);
+  d.t1 = __ldg(p.cu_seqlens + d.b + 1);
+  d.range_ok = d.t0 >= 0 && d.t1 >= d.t0 && d.t1 <= p.T;
+  d.slot_ok = d.slot >= 0 && d.slot < p.max_slots;
+  return d;
+}
+
+__device__ __forceinline__ float* tile_ptr(const DecodeArgs& p, const Item& d) {
+  return p.state_pool + ((size_t)d.slot * p.HV + d.hv) * (size_t)(kHeadDim * kHeadDim);
+}
+
+// Arrive on the ring slot for `item`, start its tile copy when it has one,
+// and leave its descriptor beside the slot for the other threads.
+__device__ __forceinline__ void issue_item(const DecodeArgs& p, long long item, float* dst,
+                                           uint64_t* bar, Item* desc) {
+  const Item d = load_item(p, item);
+  *desc = d;
+  const bool copy = d.has_tile();
+  mbar_expect_tx(bar, copy ? kTileBytes : 0u);
+  if (copy) bulk_load(dst, tile_ptr(p, d), kTileBytes, bar);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) kda_decode_kernel(const DecodeArgs p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  float* ring = reinterpret_cast<float*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  TokenStage* wstage = reinterpret_cast<TokenStage*>(ring + kBufs * kHeadDim * kHeadDim);
+  Item* descs = reinterpret_cast<Item*>(wstage + kWarps);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(descs + kBufs);
+
   const int lane = threadIdx.x & 31;
-
-  const int slot = p.state_indices[b];
-  const int t0 = p.cu_seqlens[b];
-  const int t1 = p.cu_seqlens[b + 1];
-
-  if (item == 0 && threadIdx.x == 0 && (p.cu_seqlens[0] != 0 || p.cu_seqlens[p.B] != p.T))
-    raise_status(p.dev_status, KDA_DEV_BAD_SEQLEN);
-  if (t0 < 0 || t1 < t0 || t1 > p.T) {
-    if (hv == 0 && threadIdx.x == 0) raise_status(p.dev_status, KDA_DEV_BAD_SEQLEN);
-    return;
-  }
-  if (slot < 0 || slot >= p.max_slots) {
-    if (slot >= p.max_slots && hv == 0 && threadIdx.x == 0)
-      raise_status(p.dev_status, KDA_DEV_BAD_SLOT);
-    const int quads = (t1 - t0) * (kHeadDim / 4);
-    for (int i = threadIdx.x; i < quads; i += kThreads) {
-      const int t = t0 + i / (kHeadDim / 4);
-      const int c = (i % (kHeadDim / 4)) * 4;
-      *reinterpret_cast<float4*>(p.output + ((size_t)t * p.HV + hv) * kHeadDim + c) =
-          make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    return;
-  }
-  if (t1 == t0) return;  // nothing to advance: state left bit-identical
-
   const TileLane tl = tile_lane();
-  float* tile = p.state_pool + ((size_t)slot * p.HV + hv) * (size_t)(kHeadDim * kHeadDim);
-  float4 s[16];
-  tile_load(s, tile, tl);
+  TokenStage& ts = wstage[threadIdx.x >> 5];
+  const long long items = (long long)p.B * p.HV;
+  const long long G = gridDim.x;
+  const long long first = blockIdx.x;
+  const int nmine = items > first ? (int)((items - first + G - 1) / G) : 0;
 
-  const int h = hv / p.G;
-  const float a_exp = expf(p.a_log[hv]);
-
-  for (int c0 = t0; c0 < t1; c0 += kChunk) {
-    const int nc = min(kChunk, t1 - c0);
-    if (c0 != t0) __syncthreads();  // the previous round's stage is consumed
-    if (warp < nc) stage_token(p, c0 + warp, h, hv, a_exp, p.q_scale, stage[warp], lane);
-    __syncthreads();
-    for (int j = 0; j < nc; ++j) {
-      const float4 o = tile_token_step(s, stage[j], tl);
-      if (tl.rg == 0)
-        __stcs(reinterpret_cast<float4*>(p.output + ((size_t)(c0 + j) * p.HV + hv) * kHeadDim + tl.col), o);
-    }
+  if (blockIdx.x == 0 && threadIdx.x == 0 &&
+      (p.cu_seqlens[0] != 0 || p.cu_seqlens[p.B] != p.T))
+    raise_status(p.dev_status, KDA_DEV_BAD_SEQLEN);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kBufs; ++i) mbar_init(&bars[i], 1);
+    mbar_fence_init();
+    for (int j = 0; j < kBufs && j < nmine; ++j)
+      issue_item(p, first + j * G, ring + j * kHeadDim * kHeadDim, &bars[j], &descs[j]);
   }
-  tile_store(tile, s, tl);
+  __syncthreads();
+
+  // Inputs of the first token of the next item, fetched one item ahead.
+  TokenIn cur = {};
+  if (nmine > 0 && descs[0].has_tile())
+    cur = fetch_token(p, descs[0].t0, descs[0].hv / p.G, descs[0].hv, lane);
+
+  int j = 0;
+  for (; j < nmine; ++j) {
+    const int buf = j % kBufs;
+    const Item d = descs[buf];
+    const bool tile = d.has_tile();
+    const int h = d.hv / p.G;
+    __syncwarp();  // the warp is done with the previous item's record
+    if (tile) build_stage(p, cur, ts, lane);
+    if (j + 1 < nmine) {
+      const Item dn = descs[(j + 1) % kBufs];
+      if (dn.has_tile()) cur = fetch_token(p, dn.t0, dn.hv / p.G, dn.hv, lane);
+    }
+
+    const bool arrived = mbar_wait(&bars[buf], (uint32_t)(j / kBufs) & 1u);
+    float4 s[16];
+    if (tile && arrived) {
+      const float* src = ring + buf * kHeadDim * kHeadDim;
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        s[i] = *reinterpret_cast<const float4*>(src + (tl.rg + 8 * i) * kHeadDim + tl.col);
+    }
+    // Every thread has read the slot and its descriptor: the slot can take
+    // the tile of item j + kBufs.
+    if (__syncthreads_or(!arrived)) break;
+    if (threadIdx.x == 0 && j + kBufs < nmine)
+      issue_item(p, first + (long long)(j + kBufs) * G, ring + buf * kHeadDim * kHeadDim,
+                 &bars[buf], &descs[buf]);
+
+    if (!d.range_ok) {
+      if (d.hv == 0 && threadIdx.x == 0) raise_status(p.dev_status, KDA_DEV_BAD_SEQLEN);
+      continue;
+    }
+    if (!d.slot_ok) {
+      if (d.slot >= p.max_slots && d.hv == 0 && threadIdx.x == 0)
+        raise_status(p.dev_status, KDA_DEV_BAD_SLOT);
+      const int quads = (d.t1 - d.t0) * (kHeadDim / 4);
+      for (int i = threadIdx.x; i < quads; i += kThreads) {
+        const int t = d.t0 + i / (kHeadDim / 4);
+        const int c = (i % (kHeadDim / 4)) * 4;
+        *reinterpret_cast<float4*>(p.output + ((size_t)t * p.HV + d.hv) * kHeadDim + c) =
+            make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      continue;
+    }
+    if (!tile) continue;  // no tokens: the state stays bit-identical
+
+    TokenIn nxt = {};
+    if (d.t0 + 1 < d.t1) nxt = fetch_token(p, d.t0 + 1, h, d.hv, lane);
+    for (int t = d.t0; t < d.t1; ++t) {
+      if (t != d.t0) {
+        __syncwarp();  // every lane is done with the previous token's record
+        build_stage(p, nxt, ts, lane);
+        if (t + 1 < d.t1) nxt = fetch_token(p, t + 1, h, d.hv, lane);
+      }
+      __syncwarp();
+      const float4 o = tile_token_step(s, ts, tl);
+      if (tl.rg == 0)
+        __stcs(reinterpret_cast<float4*>(p.output + ((size_t)t * p.HV + d.hv) * kHeadDim + tl.col), o);
+    }
+    tile_store(tile_ptr(p, d), s, tl);
+  }
+
+  if (j < nmine) {
+    // A ring wait gave up: record it and let the copies already issued land
+    // (bounded) before the CTA's shared memory is released.
+    if (threadIdx.x == 0) {
+      raise_status(p.dev_status, KDA_DEV_TIMEOUT);
+      for (int k = j; k < j + kBufs && k < nmine; ++k)
+        mbar_wait(&bars[k % kBufs], (uint32_t)(k / kBufs) & 1u);
+    }
+    __syncthreads();
+  }
 }
 
 }  // namespace
 
+size_t decode_smem_bytes() {
+  return 128 + (size_t)kBufs * kTileBytes + kWarps * sizeof(TokenStage) + kBufs * sizeof(Item) +
+         kBufs * sizeof(uint64_t);
+}
+
 cudaError_t launch_kda_decode(const DecodeArgs& args, cudaStream_t stream) {
   const long long items = (long long)args.B * args.HV;
   if (items == 0) return cudaSuccess;
-  kda_decode_kernel<<<(unsigned)items, kThreads, 0, stream>>>(args);
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const size_t smem = decode_smem_bytes();
+  e = cudaFuncSetAttribute(kda_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const long long grid = items < sms ? items : sms;
+  kda_decode_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(args);
   return cudaGetLastError();
 }
 

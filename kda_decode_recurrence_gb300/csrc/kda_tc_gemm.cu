@@ -23,6 +23,7 @@
 // timer; on expiry the CTA records an error bit and returns cleanly.
 #include <cuda.h>
 
+#include "kda_async.cuh"
 #include "kda_common.cuh"
 #include "kda_launch.h"
 #include "kda_tc_gemm.h"
@@ -35,44 +36,6 @@ constexpr int kBK = 64;                  // contraction rows per stage
 constexpr int kTileN = 128;              // weight columns per CTA (MMA M)
 constexpr int kABytes = kBK * kTileN * 2;  // 16 KiB: two 64x64 swizzled boxes
 constexpr int kBoxRows = 32;             // token rows per TMA box of X2
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-// Wait until the phase with the given parity has completed; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  const uint32_t addr = smem_u32(bar);
-  const unsigned long long t0 = global_ns();
-  while (true) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(addr), "r"(parity)
-        : "memory");
-    if (done) return true;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
-  }
-}
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int x, int y) {
@@ -256,7 +219,7 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
   // reads TMEM only if all of its lanes saw the accumulator complete.
   const bool have = __all_sync(0xffffffffu, mbar_wait(done, 0)) != 0;
   if (!have || !ok) {
-    if (lane == 0) atomicOr(err, 1);
+    if (lane == 0) atomicOr(err, KDA_DEV_TIMEOUT);
   }
   tc_fence_after();
   const int m = n0 + warp * 32 + lane;

@@ -154,3 +154,39 @@ def test_lower_bound_gate_never_amplifies_on_gpu():
     slots = inp["state_indices"].long()
     ratio = (pool[slots.cuda()].cpu() / inp["state_pool"][slots]).numpy()
     assert np.all(ratio <= 1.0) and np.all(ratio >= np.exp(-5.0) * (1 - 1e-6))
+
+
+def test_persistent_ring_with_mixed_items():
+    # Many more (request, head) items than SMs, so every CTA cycles through its
+    # copy ring many times, with padded, out-of-range and empty requests mixed
+    # in (their ring slots are consumed without a tile).
+    rng = np.random.default_rng(77)
+    B, HV, N = 400, 2, 430
+    lengths = rng.integers(0, 4, size=B)
+    inp = decode_inputs("varlen", B=B, H=1, HV=HV, max_slots=N, lengths=lengths, seed=78)
+    idx = inp["state_indices"].numpy().copy()
+    padded = rng.choice(B, size=30, replace=False)
+    idx[padded[:20]] = -1
+    idx[padded[20:]] = N + 5                      # out of range
+    inp["state_indices"] = torch.from_numpy(idx)
+    d = to_device(inp)
+    before = d["state_pool"].clone()
+    out = torch.full((inp["T"], HV, 128), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda_decode(out, d["q"], d["k"], d["v"], d["raw_gate"], d["beta_logits"], d["a_log"],
+               d["dt_bias"], d["cu_seqlens"], d["state_pool"], d["state_indices"],
+               gate_mode=inp["gate_mode"], lower_bound=inp["lower_bound"], dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == DEV_BAD_SLOT
+    cu = inp["cu_seqlens"].numpy()
+    o = out.cpu().numpy()
+    for b in padded:
+        assert np.all(o[cu[b]:cu[b + 1]] == 0.0)
+    valid = [b for b in range(B) if idx[b] >= 0 and idx[b] < N]
+    rows, slots, ref_out, ref_pool = oracle_decode_sample(inp, valid)
+    assert_outputs_close(o[rows], ref_out)
+    assert_states_close(d["state_pool"][torch.from_numpy(slots.astype(np.int64)).cuda()].cpu().numpy(),
+                        ref_pool)
+    advanced = set(int(idx[b]) for b in valid if lengths[b] > 0)
+    untouched = torch.tensor([s for s in range(N) if s not in advanced], device="cuda")
+    assert torch.equal(d["state_pool"][untouched], before[untouched])
