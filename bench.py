@@ -46,8 +46,8 @@ FALLBACK_HBM_GBS = 6800.0
 # profiles/), tied to the kernel sources they were taken with: when the
 # sources change the figure no longer describes the kernel and is reported
 # as null.
-NCU_TRAFFIC = {"sources_sha256": "18a38e0626ef46c274229acf3081792f8a00b789ce3673a3f556db98f94f84c7",
-               "bytes_per_launch": 1.64e9 + 1.58e9}  # read + write, grouped workload
+NCU_TRAFFIC = {"sources_sha256": "deb0b3b9ee59f9300e2ddf536bfccfe87003c865dc097362f9b3533add58c56e",
+               "bytes_per_launch": 1636034304 + 1566834176}  # read + write, grouped workload
 
 
 def kernel_sources_sha() -> str:
@@ -316,6 +316,40 @@ def run_block(steps: int, warmup: int) -> dict:
             "state_updates_per_s": cfg.B * cfg.nh / t}
 
 
+def run_decode_variant(inp: dict, d: dict, steps: int) -> dict:
+    """kda_decode_ex on the same workload with the transposed (V-first) state
+    and bf16 output, timed like the main step (CUDA events per launch)."""
+    from kda_decode_recurrence_gb300 import STATE_V_FIRST, kda_decode_ex
+    T, H, HV, K, V, B = inp["T"], inp["H"], inp["HV"], inp["K"], inp["V"], inp["B"]
+    pool = d["state_pool"].transpose(-1, -2).contiguous()
+    out = torch.empty(T, HV, V, dtype=torch.bfloat16, device=pool.device)
+    stream = torch.cuda.current_stream(pool.device)
+
+    def call():
+        kda_decode_ex(out, d["q"], d["k"], d["v"], d["raw_gate"], d["beta_logits"], d["a_log"],
+                      d["dt_bias"], d["cu_seqlens"], pool, d["state_indices"],
+                      gate_mode=inp["gate_mode"], lower_bound=inp["lower_bound"],
+                      state_layout=STATE_V_FIRST, stream=stream)
+
+    for _ in range(3):
+        call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for s_, e_ in ev:
+        s_.record(stream)
+        call()
+        e_.record(stream)
+    torch.cuda.synchronize(pool.device)
+    t = sum(s_.elapsed_time(e_) for s_, e_ in ev) * 1e-3 / steps
+    nbytes = decode_bytes(B, T, H, HV, K, V) - T * HV * V * 2   # bf16 output
+    peak, src = measured_peaks()
+    del pool
+    return {"workload": "same as config, state_layout V_FIRST ([V, K] tiles), bf16 output",
+            "us_per_launch": t * 1e6, "launches": steps, "algorithmic_bytes": nbytes,
+            "achieved_gbs": nbytes / t / 1e9, "frac_of_hbm_peak": nbytes / t / 1e9 / peak,
+            "peak_source": src, "state_updates_per_s": T * HV / t}
+
+
 def run_gpu(args, rank, world, local):
     from kda_decode_recurrence_gb300 import kda_decode
     cfg = DECODE_CONFIGS[WORKLOAD]
@@ -396,6 +430,7 @@ def run_gpu(args, rank, world, local):
     e2e_value = world * updates_per_step * e2e_steps / e2e_elapsed
 
     block = run_block(steps=max(5, min(args.steps, 50)), warmup=3) if rank == 0 else None
+    variant = run_decode_variant(inp, d, steps=max(5, min(args.steps, 200))) if rank == 0 else None
 
     if rank != 0:
         return
@@ -428,6 +463,7 @@ def run_gpu(args, rank, world, local):
         "clocks": clocks,
         "cpu_baseline": cpu,
         "block_tkg": block,
+        "decode_v_first_bf16": variant,
     }
     print(json.dumps(line), flush=True)
 

@@ -52,7 +52,7 @@ typedef enum kda_status {
   KDA_ERR_NULL = -1,        /* a required pointer is NULL                         */
   KDA_ERR_SHAPE = -2,       /* a size is out of range or sizes are inconsistent  */
   KDA_ERR_UNSUPPORTED = -3, /* valid sizes this build does not implement         */
-  KDA_ERR_ENUM = -4,        /* unknown gate_mode                                  */
+  KDA_ERR_ENUM = -4,        /* unknown gate_mode, state_layout or output_dtype   */
   KDA_ERR_CUDA = -5,        /* a CUDA runtime call (launch) failed                */
   KDA_ERR_ALIGN = -6,       /* a pointer is not aligned as documented             */
   KDA_ERR_VALUE = -7,       /* a scalar argument is not finite / out of range     */
@@ -127,6 +127,34 @@ kda_status kda_decode(float* output, const kda_bf16* q, const kda_bf16* k, const
                       const int32_t* state_indices, int gate_mode, float lower_bound, int B,
                       int T, int H, int HV, int K, int V, int max_slots, int32_t* dev_status,
                       void* stream);
+
+/* state_layout and output_dtype values of kda_decode_ex.  "KdaDecode", execute:
+ * the state_layout and output_dtype template parameters; "Delta-rule write",
+ * attention forward: the model keeps its state transposed
+ * (transpose_state_layout=True). */
+#define KDA_STATE_K_FIRST 0 /* tile [K, V], row k contiguous over v (kda_decode) */
+#define KDA_STATE_V_FIRST 1 /* tile [V, K], row v contiguous over k (the transposed state) */
+#define KDA_OUTPUT_F32 0
+#define KDA_OUTPUT_BF16 1
+
+/*
+ * kda_decode_ex -- kda_decode with the state layout and output dtype chosen
+ * at run time.  Same operation, arguments and error behaviour as kda_decode,
+ * except:
+ *   output        [T, HV, V] fp32 (KDA_OUTPUT_F32, alignment 16 B) or bf16
+ *                 (KDA_OUTPUT_BF16, round to nearest even, alignment 8 B).
+ *   state_pool    [max_slots, HV, K, V] (KDA_STATE_K_FIRST) or
+ *                 [max_slots, HV, V, K] (KDA_STATE_V_FIRST) fp32.
+ *   state_layout, output_dtype  the enums above; anything else returns
+ *                 KDA_ERR_ENUM.
+ * kda_decode(...) is kda_decode_ex(..., KDA_STATE_K_FIRST, KDA_OUTPUT_F32, ...).
+ */
+kda_status kda_decode_ex(void* output, const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
+                         const float* raw_gate, const float* beta_logits, const float* a_log,
+                         const float* dt_bias, const int32_t* cu_seqlens, float* state_pool,
+                         const int32_t* state_indices, int gate_mode, float lower_bound,
+                         int state_layout, int output_dtype, int B, int T, int H, int HV, int K,
+                         int V, int max_slots, int32_t* dev_status, void* stream);
 
 /*
  * kda_block_tkg -- the fused KDA block for token generation.

@@ -19,6 +19,10 @@ from . import _lib
 
 GATE_SOFTPLUS = 0
 GATE_LOWER_BOUND = 1
+STATE_K_FIRST = 0
+STATE_V_FIRST = 1
+OUTPUT_F32 = 0
+OUTPUT_BF16 = 1
 DEV_BAD_SLOT = 1
 DEV_BAD_SEQLEN = 2
 
@@ -85,6 +89,47 @@ def kda_decode(output, q, k, v, raw_gate, beta_logits, a_log, dt_bias, cu_seqlen
         _stream_handle(stream))
     if check and rc != 0:
         raise KdaError(rc, "kda_decode")
+    return rc
+
+
+def kda_decode_ex(output, q, k, v, raw_gate, beta_logits, a_log, dt_bias, cu_seqlens, state_pool,
+                  state_indices, gate_mode=GATE_SOFTPLUS, lower_bound=-5.0,
+                  state_layout=STATE_K_FIRST, dev_status=None, stream=None, check=True) -> int:
+    """kda_decode with a chosen state layout (STATE_K_FIRST: tiles [K, V];
+    STATE_V_FIRST: tiles [V, K]) and the output dtype taken from ``output``
+    (float32 or bfloat16)."""
+    dev = state_pool.device
+    T = q.shape[-3]
+    H, K = q.shape[-2], q.shape[-1]
+    HV, V = v.shape[-2], v.shape[-1]
+    B = state_indices.shape[0]
+    N = state_pool.shape[0]
+    if output.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError(f"output: expected float32 or bfloat16, got {output.dtype}")
+    out_dtype = OUTPUT_F32 if output.dtype == torch.float32 else OUTPUT_BF16
+    _check(output, "output", output.dtype, dev)
+    for t, n, dt in ((q, "q", torch.bfloat16), (k, "k", torch.bfloat16), (v, "v", torch.bfloat16),
+                     (raw_gate, "raw_gate", torch.float32),
+                     (beta_logits, "beta_logits", torch.float32), (a_log, "a_log", torch.float32),
+                     (dt_bias, "dt_bias", torch.float32), (cu_seqlens, "cu_seqlens", torch.int32),
+                     (state_pool, "state_pool", torch.float32),
+                     (state_indices, "state_indices", torch.int32)):
+        _check(t, n, dt, dev)
+    tile = (K, V) if state_layout == STATE_K_FIRST else (V, K)
+    if tuple(state_pool.shape[1:]) != (HV, *tile):
+        raise ValueError(f"state_pool shape {tuple(state_pool.shape)} != [N, {HV}, {tile[0]}, {tile[1]}]")
+    if cu_seqlens.numel() != B + 1:
+        raise ValueError("cu_seqlens must have B + 1 entries")
+    if dev_status is not None:
+        _check(dev_status, "dev_status", torch.int32, dev)
+    rc = _lib.load().kda_decode_ex(
+        output.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), raw_gate.data_ptr(),
+        beta_logits.data_ptr(), a_log.data_ptr(), dt_bias.data_ptr(), cu_seqlens.data_ptr(),
+        state_pool.data_ptr(), state_indices.data_ptr(), int(gate_mode), float(lower_bound),
+        int(state_layout), out_dtype, B, T, H, HV, K, V, N,
+        None if dev_status is None else dev_status.data_ptr(), _stream_handle(stream))
+    if check and rc != 0:
+        raise KdaError(rc, "kda_decode_ex")
     return rc
 
 

@@ -14,8 +14,8 @@ _lock = threading.Lock()
 _lib = None
 
 # Every symbol include/kda.h declares.
-EXPORTS = ("kda_decode", "kda_block_tkg", "kda_block_tkg_static", "kda_block_tkg_workspace_size",
-           "kda_status_string", "kda_version")
+EXPORTS = ("kda_decode", "kda_decode_ex", "kda_block_tkg", "kda_block_tkg_static",
+           "kda_block_tkg_workspace_size", "kda_status_string", "kda_version")
 
 STATUS = {
     0: "KDA_OK", -1: "KDA_ERR_NULL", -2: "KDA_ERR_SHAPE", -3: "KDA_ERR_UNSUPPORTED",
@@ -28,6 +28,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.kda_decode.restype = i
     lib.kda_decode.argtypes = [vp] * 11 + [i, f] + [i] * 7 + [vp, vp]
+    lib.kda_decode_ex.restype = i
+    lib.kda_decode_ex.argtypes = [vp] * 11 + [i, f, i, i] + [i] * 7 + [vp, vp]
     lib.kda_block_tkg.restype = i
     lib.kda_block_tkg.argtypes = [vp] * 13 + [f] * 4 + [i] * 7 + [vp, ctypes.c_size_t, vp, vp]
     lib.kda_block_tkg_static.restype = i

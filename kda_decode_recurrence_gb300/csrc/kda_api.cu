@@ -20,7 +20,7 @@ const char* kda_status_string(kda_status status) {
     case KDA_ERR_NULL: return "a required pointer is NULL";
     case KDA_ERR_SHAPE: return "a size is out of range or sizes are inconsistent";
     case KDA_ERR_UNSUPPORTED: return "sizes not implemented by this build";
-    case KDA_ERR_ENUM: return "unknown gate_mode";
+    case KDA_ERR_ENUM: return "unknown gate_mode, state_layout or output_dtype";
     case KDA_ERR_CUDA: return "a CUDA runtime call failed";
     case KDA_ERR_ALIGN: return "a pointer is not aligned as documented";
     case KDA_ERR_VALUE: return "a scalar argument is not finite or out of range";
@@ -31,15 +31,21 @@ const char* kda_status_string(kda_status status) {
 
 const char* kda_version(void) { return "kda-gb300 0.1"; }
 
-kda_status kda_decode(float* output, const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
-                      const float* raw_gate, const float* beta_logits, const float* a_log,
-                      const float* dt_bias, const int32_t* cu_seqlens, float* state_pool,
-                      const int32_t* state_indices, int gate_mode, float lower_bound, int B,
-                      int T, int H, int HV, int K, int V, int max_slots, int32_t* dev_status,
-                      void* stream) {
+}  // extern "C"
+
+namespace {
+
+kda_status decode_impl(void* output, const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
+                       const float* raw_gate, const float* beta_logits, const float* a_log,
+                       const float* dt_bias, const int32_t* cu_seqlens, float* state_pool,
+                       const int32_t* state_indices, int gate_mode, float lower_bound,
+                       int state_layout, int output_dtype, int B, int T, int H, int HV, int K,
+                       int V, int max_slots, int32_t* dev_status, void* stream) {
   if (B < 0 || T < 0 || H < 1 || HV < 1 || K < 1 || V < 1 || max_slots < 1) return KDA_ERR_SHAPE;
   if (HV % H != 0) return KDA_ERR_SHAPE;
   if (gate_mode != KDA_GATE_SOFTPLUS && gate_mode != KDA_GATE_LOWER_BOUND) return KDA_ERR_ENUM;
+  if (state_layout != KDA_STATE_K_FIRST && state_layout != KDA_STATE_V_FIRST) return KDA_ERR_ENUM;
+  if (output_dtype != KDA_OUTPUT_F32 && output_dtype != KDA_OUTPUT_BF16) return KDA_ERR_ENUM;
   if (gate_mode == KDA_GATE_LOWER_BOUND && !(std::isfinite(lower_bound) && lower_bound <= 0.0f))
     return KDA_ERR_VALUE;
   if (K != kda::kHeadDim || V != kda::kHeadDim) return KDA_ERR_UNSUPPORTED;
@@ -50,7 +56,8 @@ kda_status kda_decode(float* output, const kda_bf16* q, const kda_bf16* k, const
   if (!aligned(state_pool, 16) || !aligned(dt_bias, 16) || !aligned(cu_seqlens, 4) ||
       !aligned(state_indices, 4) || !aligned(a_log, 4))
     return KDA_ERR_ALIGN;
-  if (T > 0 && (!aligned(output, 16) || !aligned(raw_gate, 16) || !aligned(q, 8) ||
+  const uintptr_t out_align = output_dtype == KDA_OUTPUT_F32 ? 16 : 8;
+  if (T > 0 && (!aligned(output, out_align) || !aligned(raw_gate, 16) || !aligned(q, 8) ||
                 !aligned(k, 8) || !aligned(v, 8) || !aligned(beta_logits, 4)))
     return KDA_ERR_ALIGN;
 
@@ -70,6 +77,8 @@ kda_status kda_decode(float* output, const kda_bf16* q, const kda_bf16* k, const
   a.gate_mode = gate_mode;
   a.lower_bound = lower_bound;
   a.q_scale = 1.0f / std::sqrt((float)K);
+  a.v_first = state_layout == KDA_STATE_V_FIRST;
+  a.out_bf16 = output_dtype == KDA_OUTPUT_BF16;
   a.B = B;
   a.T = T;
   a.H = H;
@@ -79,6 +88,32 @@ kda_status kda_decode(float* output, const kda_bf16* q, const kda_bf16* k, const
   if (kda::launch_kda_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return KDA_ERR_CUDA;
   return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_decode(float* output, const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
+                      const float* raw_gate, const float* beta_logits, const float* a_log,
+                      const float* dt_bias, const int32_t* cu_seqlens, float* state_pool,
+                      const int32_t* state_indices, int gate_mode, float lower_bound, int B,
+                      int T, int H, int HV, int K, int V, int max_slots, int32_t* dev_status,
+                      void* stream) {
+  return decode_impl(output, q, k, v, raw_gate, beta_logits, a_log, dt_bias, cu_seqlens,
+                     state_pool, state_indices, gate_mode, lower_bound, KDA_STATE_K_FIRST,
+                     KDA_OUTPUT_F32, B, T, H, HV, K, V, max_slots, dev_status, stream);
+}
+
+kda_status kda_decode_ex(void* output, const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
+                         const float* raw_gate, const float* beta_logits, const float* a_log,
+                         const float* dt_bias, const int32_t* cu_seqlens, float* state_pool,
+                         const int32_t* state_indices, int gate_mode, float lower_bound,
+                         int state_layout, int output_dtype, int B, int T, int H, int HV, int K,
+                         int V, int max_slots, int32_t* dev_status, void* stream) {
+  return decode_impl(output, q, k, v, raw_gate, beta_logits, a_log, dt_bias, cu_seqlens,
+                     state_pool, state_indices, gate_mode, lower_bound, state_layout,
+                     output_dtype, B, T, H, HV, K, V, max_slots, dev_status, stream);
 }
 
 size_t kda_block_tkg_workspace_size(int B, int n, int Hd, int nh, int K, int V, int Kc) {

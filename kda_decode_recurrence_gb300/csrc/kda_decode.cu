@@ -130,6 +130,26 @@ __device__ __forceinline__ void issue_item(const DecodeArgs& p, long long item, 
   if (copy) bulk_load(dst, tile_ptr(p, d), kTileBytes, bar);
 }
 
+// Output row of token t, value head hv: 4 consecutive values from column col.
+template <bool kOutBf16>
+__device__ __forceinline__ void store_out(const DecodeArgs& p, int t, int hv, int col, float4 o) {
+  const size_t off = ((size_t)t * p.HV + hv) * kHeadDim + col;
+  if (kOutBf16) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(o.z, o.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+    __stcs(reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.output) + off), pk);
+  } else {
+    __stcs(reinterpret_cast<float4*>(static_cast<float*>(p.output) + off), o);
+  }
+}
+
+// kVFirst: tiles are stored [V, K] (row v contiguous over k, the layout of a
+// transposed state); the register tile is still S[k][v], so the element
+// (k, v) is read from and written to v * 128 + k.
+template <bool kVFirst, bool kOutBf16>
 __global__ void __launch_bounds__(kThreads, 1) kda_decode_kernel(const DecodeArgs p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   float* ring = reinterpret_cast<float*>(
@@ -179,9 +199,18 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_kernel(const DecodeArg
     float4 s[16];
     if (tile && arrived) {
       const float* src = ring + buf * kHeadDim * kHeadDim;
+      if (kVFirst) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        s[i] = *reinterpret_cast<const float4*>(src + (tl.rg + 8 * i) * kHeadDim + tl.col);
+        for (int i = 0; i < 16; ++i) {
+          const int r = tl.rg + 8 * i;
+          s[i] = make_float4(src[(tl.col + 0) * kHeadDim + r], src[(tl.col + 1) * kHeadDim + r],
+                             src[(tl.col + 2) * kHeadDim + r], src[(tl.col + 3) * kHeadDim + r]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          s[i] = *reinterpret_cast<const float4*>(src + (tl.rg + 8 * i) * kHeadDim + tl.col);
+      }
     }
     // Every thread has read the slot and its descriptor: the slot can take
     // the tile of item j + kBufs.
@@ -198,12 +227,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_kernel(const DecodeArg
       if (d.slot >= p.max_slots && d.hv == 0 && threadIdx.x == 0)
         raise_status(p.dev_status, KDA_DEV_BAD_SLOT);
       const int quads = (d.t1 - d.t0) * (kHeadDim / 4);
-      for (int i = threadIdx.x; i < quads; i += kThreads) {
-        const int t = d.t0 + i / (kHeadDim / 4);
-        const int c = (i % (kHeadDim / 4)) * 4;
-        *reinterpret_cast<float4*>(p.output + ((size_t)t * p.HV + d.hv) * kHeadDim + c) =
-            make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+      for (int i = threadIdx.x; i < quads; i += kThreads)
+        store_out<kOutBf16>(p, d.t0 + i / (kHeadDim / 4), d.hv, (i % (kHeadDim / 4)) * 4,
+                            make_float4(0.f, 0.f, 0.f, 0.f));
       continue;
     }
     if (!tile) continue;  // no tokens: the state stays bit-identical
@@ -218,10 +244,22 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_kernel(const DecodeArg
       }
       __syncwarp();
       const float4 o = tile_token_step(s, ts, tl);
-      if (tl.rg == 0)
-        __stcs(reinterpret_cast<float4*>(p.output + ((size_t)t * p.HV + d.hv) * kHeadDim + tl.col), o);
+      if (tl.rg == 0) store_out<kOutBf16>(p, t, d.hv, tl.col, o);
     }
-    tile_store(tile_ptr(p, d), s, tl);
+    float* dst = tile_ptr(p, d);
+    if (kVFirst) {
+      // Each instruction writes 4 runs of 8 consecutive floats (full sectors).
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int r = tl.rg + 8 * i;
+        __stcs(dst + (tl.col + 0) * kHeadDim + r, s[i].x);
+        __stcs(dst + (tl.col + 1) * kHeadDim + r, s[i].y);
+        __stcs(dst + (tl.col + 2) * kHeadDim + r, s[i].z);
+        __stcs(dst + (tl.col + 3) * kHeadDim + r, s[i].w);
+      }
+    } else {
+      tile_store(dst, s, tl);
+    }
   }
 
   if (j < nmine) {
@@ -252,10 +290,13 @@ cudaError_t launch_kda_decode(const DecodeArgs& args, cudaStream_t stream) {
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const size_t smem = decode_smem_bytes();
-  e = cudaFuncSetAttribute(kda_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  void (*kernel)(DecodeArgs) =
+      args.v_first ? (args.out_bf16 ? kda_decode_kernel<true, true> : kda_decode_kernel<true, false>)
+                   : (args.out_bf16 ? kda_decode_kernel<false, true> : kda_decode_kernel<false, false>);
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const long long grid = items < sms ? items : sms;
-  kda_decode_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(args);
+  kernel<<<(unsigned)grid, kThreads, smem, stream>>>(args);
   return cudaGetLastError();
 }
 

@@ -15,7 +15,7 @@ namespace kda {
 constexpr int kHeadDim = 128;
 
 struct DecodeArgs {
-  float* output;
+  void* output;  // fp32 or bf16 [T, HV, V] (out_bf16)
   const kda_bf16* q;
   const kda_bf16* k;
   const kda_bf16* v;
@@ -30,6 +30,8 @@ struct DecodeArgs {
   int gate_mode;
   float lower_bound;
   float q_scale;  // K^-1/2
+  int v_first;    // state tiles stored [V, K] instead of [K, V]
+  int out_bf16;   // output written as bf16
   int B, T, H, HV, G, max_slots;
 };
 

@@ -111,3 +111,21 @@ def test_block_workspace_size(lib):
     assert lib.kda_block_tkg_workspace_size(64, 1, 4096, 32, 128, 128, 4) > ws
     assert lib.kda_block_tkg_workspace_size(32, 2, 4096, 32, 128, 128, 4) == 0
     assert lib.kda_block_tkg_workspace_size(32, 1, 4096, 12, 128, 128, 4) == 0
+
+
+def decode_ex_args(**kw):
+    a = dict(output=P, q=P, k=P, v=P, raw_gate=P, beta_logits=P, a_log=P, dt_bias=P,
+             cu_seqlens=P, state_pool=P, state_indices=P, gate_mode=0, lower_bound=-5.0,
+             state_layout=0, output_dtype=0, B=2, T=3, H=2, HV=4, K=128, V=128, max_slots=8,
+             dev_status=None, stream=None)
+    a.update(kw)
+    return list(a.values())
+
+
+@pytest.mark.parametrize("kw,expect", [
+    ({"state_layout": 2}, ERR_ENUM), ({"output_dtype": 2}, ERR_ENUM), ({"state_layout": -1}, ERR_ENUM),
+    ({"output_dtype": 0, "output": P + 8}, ERR_ALIGN), ({"output_dtype": 1, "output": P + 4}, ERR_ALIGN),
+    ({"B": 0, "state_layout": 1, "output_dtype": 1}, KDA_OK), ({"K": 64}, ERR_UNSUP),
+])
+def test_decode_ex_host_validation(lib, kw, expect):
+    assert lib.kda_decode_ex(*decode_ex_args(**kw)) == expect

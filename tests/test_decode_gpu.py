@@ -190,3 +190,49 @@ def test_persistent_ring_with_mixed_items():
     advanced = set(int(idx[b]) for b in valid if lengths[b] > 0)
     untouched = torch.tensor([s for s in range(N) if s not in advanced], device="cuda")
     assert torch.equal(d["state_pool"][untouched], before[untouched])
+
+
+# ------------------------------------------------ kda_decode_ex (layout, dtype)
+
+from kda_decode_recurrence_gb300 import STATE_V_FIRST, kda_decode_ex  # noqa: E402
+
+
+def run_ex(inp, v_first, out_dtype, dev="cuda"):
+    d = to_device(inp, dev)
+    pool = d["state_pool"].transpose(-1, -2).contiguous() if v_first else d["state_pool"]
+    out = torch.full((inp["T"], inp["HV"], inp["V"]), float("nan"), dtype=out_dtype, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    kda_decode_ex(out, d["q"], d["k"], d["v"], d["raw_gate"], d["beta_logits"], d["a_log"],
+                  d["dt_bias"], d["cu_seqlens"], pool, d["state_indices"],
+                  gate_mode=inp["gate_mode"], lower_bound=inp["lower_bound"],
+                  state_layout=STATE_V_FIRST if v_first else 0, dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    kfirst = pool.transpose(-1, -2) if v_first else pool
+    return out, kfirst
+
+
+@pytest.mark.parametrize("name", ["tiny", "varlen_small"])
+def test_v_first_and_bf16_output_match_k_first_exactly(name):
+    inp = (decode_inputs("tiny") if name == "tiny" else
+           decode_inputs("varlen", B=6, H=2, HV=4, max_slots=9, lengths=(1, 0, 9, 3, 17, 2), seed=90))
+    ref_out, ref_pool = run_ex(inp, False, torch.float32)
+    vf_out, vf_pool = run_ex(inp, True, torch.float32)
+    assert torch.equal(vf_out, ref_out) and torch.equal(vf_pool, ref_pool)
+    bf_out, bf_pool = run_ex(inp, True, torch.bfloat16)
+    rows = torch.isfinite(ref_out)
+    assert torch.equal(bf_out[rows], ref_out[rows].to(torch.bfloat16))   # round to nearest even
+    assert torch.equal(bf_pool, ref_pool)
+
+
+def test_v_first_bf16_full_size_against_oracle():
+    inp = decode_inputs("grouped")
+    out, pool = run_ex(inp, True, torch.bfloat16)
+    rng = np.random.default_rng(91)
+    bs = sorted(rng.choice(inp["B"], size=12, replace=False).tolist())
+    rows, slots, ref_out, ref_pool = oracle_decode_sample(inp, bs)
+    got = out[torch.from_numpy(rows).cuda()].float().cpu().numpy().astype(np.float64)
+    # bf16 output: the fp32 bound plus one bf16 unit in the last place (2^-8 relative)
+    err = np.abs(got - ref_out)
+    assert np.all(err <= 1e-3 * (1 + np.abs(ref_out)) + 2.0 ** -8 * np.abs(ref_out))
+    assert_states_close(pool[torch.from_numpy(slots.astype(np.int64)).cuda()].cpu().numpy(), ref_pool)
