@@ -69,14 +69,15 @@ def decode_bytes(B, T, H, HV, K, V, touched=None) -> int:
             + HV * (K + 1) * 4 + (2 * B + 1) * 4)
 
 
-def block_bytes(B, Hd, nh, K, V, Kc) -> int:
-    """Algorithmic HBM bytes of one kda_block_tkg call (n = 1): weights once,
-    S and conv_state read + written, hidden in, out out, small parameters."""
+def block_bytes(B, Hd, nh, K, V, Kc, n=1) -> int:
+    """Algorithmic HBM bytes of one kda_block_tkg call: weights once, S and
+    conv_state read + written, hidden in and out out for the B * n tokens,
+    small parameters."""
     I = 2 * K * nh + V * nh + 2 * K + nh
     weights = 2 * (Hd * I + K * K * nh + K * V * nh + 3 * Kc * K * nh + V * nh * Hd)
     params = 4 * (Hd + nh + K * nh + V)
     state = B * nh * K * V * 4 * 2 + B * 3 * K * nh * (Kc - 1) * 4 * 2
-    io = B * Hd * 4 * 2
+    io = B * n * Hd * 4 * 2
     return weights + params + state + io
 
 
@@ -276,14 +277,14 @@ def run_reference(args, rank, world):
 # --------------------------------------------------------------- GPU arm
 
 
-def run_block(steps: int, warmup: int) -> dict:
+def run_block(steps: int, warmup: int, n: int = 1) -> dict:
     from kda_decode_recurrence_gb300 import block_workspace_size, kda_block_tkg
     cfg = BLOCK_CONFIG
-    inp = block_inputs(cfg)
+    inp = block_inputs(cfg, n=n)
     dev = "cuda"
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
-    out = torch.empty(cfg.B, cfg.n, cfg.Hd, device=dev)
-    ws = torch.empty(block_workspace_size(cfg.B, cfg.n, cfg.Hd, cfg.nh, cfg.K, cfg.V, cfg.Kc),
+    out = torch.empty(cfg.B, n, cfg.Hd, device=dev)
+    ws = torch.empty(block_workspace_size(cfg.B, n, cfg.Hd, cfg.nh, cfg.K, cfg.V, cfg.Kc),
                      dtype=torch.uint8, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     names = ("hidden", "gamma_in", "W_in", "W_fb", "W_gb", "conv_w", "A_log", "dt_bias",
@@ -306,14 +307,14 @@ def run_block(steps: int, warmup: int) -> dict:
         e.synchronize()
         times.append(s.elapsed_time(e) * 1e-3)
     t = statistics.median(times)
-    nbytes = block_bytes(cfg.B, cfg.Hd, cfg.nh, cfg.K, cfg.V, cfg.Kc)
+    nbytes = block_bytes(cfg.B, cfg.Hd, cfg.nh, cfg.K, cfg.V, cfg.Kc, n)
     peak, src = measured_peaks()
-    return {"workload": f"kda_block_tkg B={cfg.B} n=1 Hd={cfg.Hd} nh={cfg.nh} dk=dv={cfg.K} "
+    return {"workload": f"kda_block_tkg B={cfg.B} n={n} Hd={cfg.Hd} nh={cfg.nh} dk=dv={cfg.K} "
                         f"Kc={cfg.Kc}, L2 flushed before each call",
-            "us_per_call": t * 1e6, "calls": steps, "gpu_launches_per_call": 6,
+            "us_per_call": t * 1e6, "calls": steps, "gpu_launches_per_call": 7,
             "algorithmic_bytes": nbytes, "achieved_gbs": nbytes / t / 1e9,
             "frac_of_hbm_peak": nbytes / t / 1e9 / peak, "peak_source": src,
-            "state_updates_per_s": cfg.B * cfg.nh / t}
+            "state_updates_per_s": cfg.B * n * cfg.nh / t}
 
 
 def run_decode_variant(inp: dict, d: dict, steps: int) -> dict:
@@ -430,6 +431,7 @@ def run_gpu(args, rank, world, local):
     e2e_value = world * updates_per_step * e2e_steps / e2e_elapsed
 
     block = run_block(steps=max(5, min(args.steps, 50)), warmup=3) if rank == 0 else None
+    block_n4 = run_block(steps=max(5, min(args.steps, 50)), warmup=3, n=4) if rank == 0 else None
     variant = run_decode_variant(inp, d, steps=max(5, min(args.steps, 200))) if rank == 0 else None
 
     if rank != 0:
@@ -463,6 +465,7 @@ def run_gpu(args, rank, world, local):
         "clocks": clocks,
         "cpu_baseline": cpu,
         "block_tkg": block,
+        "block_tkg_n4": block_n4,
         "decode_v_first_bf16": variant,
     }
     print(json.dumps(line), flush=True)

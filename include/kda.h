@@ -190,8 +190,13 @@ kda_status kda_decode_ex(void* output, const kda_bf16* q, const kda_bf16* k, con
  *   conv_state [B, 3, K*nh, Kc-1] fp32, read and advanced in place.
  *   scale, lower_bound, rms_norm_eps, l2_eps  scalars (finite; lower_bound <= 0,
  *              eps >= 0).
- *   B, n, Hd, nh, K, V, Kc  sizes.  This build implements n == 1 ("must be 1
- *              today"), K == V == 128, Kc in 2..4, Hd a multiple of 128.
+ *   B, n, Hd, nh, K, V, Kc  sizes.  n >= 1 tokens per request (the page
+ *              fixes n = 1 "today" and keeps the axis for a speculative
+ *              verify/replay window; here the n tokens of a request are taken
+ *              in order, each convolution window ending at its own token and
+ *              the state carried from token to token; out[b, j] is token j's
+ *              output).  This build implements K == V == 128, Kc in 2..4, Hd a
+ *              multiple of 128 and nh a multiple of 8.
  *   workspace  device scratch of at least kda_block_tkg_workspace_size(...)
  *              bytes, 256-byte aligned; contents need not be initialised and
  *              are clobbered.

@@ -132,7 +132,7 @@ kda_status kda_block_tkg(float* out, const float* hidden, const float* gamma_in,
         std::isfinite(rms_norm_eps) && rms_norm_eps >= 0.0f && std::isfinite(l2_eps) &&
         l2_eps >= 0.0f))
     return KDA_ERR_VALUE;
-  if (n != 1 || K != kda::kHeadDim || V != kda::kHeadDim || Kc < 2 ||
+  if (K != kda::kHeadDim || V != kda::kHeadDim || Kc < 2 ||
       Kc > 4 || Hd % 128 != 0)
     return KDA_ERR_UNSUPPORTED;
   if (B == 0) return KDA_OK;

@@ -1,11 +1,13 @@
-// kda_block.cu -- the fused KDA block for token generation (n = 1).
+// kda_block.cu -- the fused KDA block for token generation (n >= 1 tokens per
+// request).
 //
 // Operation: "KDA Block TKG Kernel API Reference" (Background; :param hidden:,
 // gamma_in, W_in, W_fb, W_gb, conv_w, A_log, dt_bias, gamma_o, W_o, out, S,
 // conv_state, scale, rms_norm_eps, lower_bound), the recurrence of "Delta-rule
 // write".
 //
-// Kernel chain on the caller's stream (rows r = b, R = B):
+// Kernel chain on the caller's stream (rows r = b * n + j for token j of request
+// b, R = B * n):
 //   1. rmsnorm      x = hidden * rsqrt(mean(hidden^2) + eps) * gamma_in, written
 //                   as bf16 hi/lo halves X2 [2R, Hd] for the tensor cores
 //   2. proj GEMM    tcgen05, P_part[ks] = x[:, split ks] . W_in[split ks, :]   [KS1, R, I]
@@ -44,7 +46,7 @@ struct Layout {
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
 bool make_layout(int B, int n, int Hd, int nh, int K, int V, int Kc, Layout* L) {
-  if (B < 1 || n != 1 || K != kHeadDim || V != kHeadDim || Kc < 2 || Kc > 4 || Hd < 128 ||
+  if (B < 1 || n < 1 || K != kHeadDim || V != kHeadDim || Kc < 2 || Kc > 4 || Hd < 128 ||
       Hd % 128 != 0 || nh < 8 || nh % 8 != 0)
     return false;
   L->R = B * n;
@@ -183,7 +185,7 @@ struct PrepArgs {
   TokenStage* stage;  // [R, nh]
   float* zgate;       // [R, nh, V]: gamma_o[d] * sigmoid(z)
   float scale, lower_bound, l2_eps;
-  int R, I, KS1, nh, Kc, CQ, CV;
+  int R, n, I, KS1, nh, Kc, CQ, CV;
 };
 
 // One channel of the depthwise causal conv: the window is conv_state[b, s, c,
@@ -199,43 +201,57 @@ __device__ __forceinline__ void conv_fetch(const PrepArgs& p, int b, int s, int 
   const int CS = p.CQ;  // channels per stream (K * nh == V * nh)
   ch.state = p.conv_state + (((size_t)b * 3 + s) * CS + c) * (p.Kc - 1);
   const unsigned short* w = reinterpret_cast<const unsigned short*>(p.conv_w) + (size_t)s * p.Kc * CS + c;
-#pragma unroll
-  for (int j = 0; j < 3; ++j) ch.win[j] = (j < p.Kc - 1) ? ch.state[j] : 0.f;
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-    ch.tap[j] = (j < p.Kc) ? __uint_as_float((uint32_t)w[(size_t)j * CS] << 16) : 0.f;
+  ch.win[0] = ch.state[0];
+  ch.win[1] = p.Kc > 2 ? ch.state[1] : 0.f;
+  ch.win[2] = p.Kc > 3 ? ch.state[2] : 0.f;
+  ch.tap[0] = __uint_as_float((uint32_t)w[0] << 16);
+  ch.tap[1] = __uint_as_float((uint32_t)w[(size_t)CS] << 16);
+  ch.tap[2] = p.Kc > 2 ? __uint_as_float((uint32_t)w[(size_t)2 * CS] << 16) : 0.f;
+  ch.tap[3] = p.Kc > 3 ? __uint_as_float((uint32_t)w[(size_t)3 * CS] << 16) : 0.f;
 }
 
-// y = SiLU(sum_j tap[j] * window[j]); the state keeps the last Kc-1 inputs.
-__device__ __forceinline__ float conv_apply(const PrepArgs& p, ConvChannel& ch, float x_new) {
-  float y = 0.f;
-#pragma unroll
-  for (int j = 0; j < 3; ++j)
-    if (j < p.Kc - 1) y = fmaf(ch.tap[j], ch.win[j], y);
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-    if (j == p.Kc - 1) y = fmaf(ch.tap[j], x_new, y);
-#pragma unroll
-  for (int j = 1; j < 3; ++j)
-    if (j < p.Kc - 1) ch.state[j - 1] = ch.win[j];
-  ch.state[p.Kc - 2] = x_new;
+// y = SiLU(sum_j tap[j] * window[j]) for the window ending at x_new, then
+// slide the window (in registers) to end at x_new.  Kc is 2, 3 or 4.
+__device__ __forceinline__ float conv_step(const PrepArgs& p, ConvChannel& ch, float x_new) {
+  float y;
+  if (p.Kc == 4) {
+    y = fmaf(ch.tap[0], ch.win[0], fmaf(ch.tap[1], ch.win[1], fmaf(ch.tap[2], ch.win[2], ch.tap[3] * x_new)));
+    ch.win[0] = ch.win[1];
+    ch.win[1] = ch.win[2];
+    ch.win[2] = x_new;
+  } else if (p.Kc == 3) {
+    y = fmaf(ch.tap[0], ch.win[0], fmaf(ch.tap[1], ch.win[1], ch.tap[2] * x_new));
+    ch.win[0] = ch.win[1];
+    ch.win[1] = x_new;
+  } else {
+    y = fmaf(ch.tap[0], ch.win[0], ch.tap[1] * x_new);
+    ch.win[0] = x_new;
+  }
   return y * sigmoidf_(y);
+}
+
+// conv_state keeps the last Kc-1 pre-convolution inputs.
+__device__ __forceinline__ void conv_save(const PrepArgs& p, const ConvChannel& ch) {
+  ch.state[0] = ch.win[0];
+  if (p.Kc > 2) ch.state[1] = ch.win[1];
+  if (p.Kc > 3) ch.state[2] = ch.win[2];
 }
 
 constexpr int kPrepHeads = 8;
 constexpr int kPrepThreads = kPrepHeads * kHeadDim;  // 1024
 
-// 4. per (request b, group of 8 heads).  q/k channels are channel-outer
-// (d * nh + h): thread t takes channel (t / 8) * nh + h0 + t % 8, so a warp
-// reads 4 runs of 8 consecutive channels.  v channels and everything per
-// (head, d) use hl = t / 128, d = t % 128 (v is head-outer, so contiguous).
+// 4. per (request b, group of 8 heads), the request's n tokens in order.
+// q/k channels are channel-outer (d * nh + h): thread t takes channel
+// (t / 8) * nh + h0 + t % 8, so a warp reads 4 runs of 8 consecutive
+// channels.  v channels and everything per (head, d) use hl = t / 128,
+// d = t % 128 (v is head-outer, so contiguous).  Each channel's conv window
+// slides across the tokens in registers and is written back once.
 __global__ void __launch_bounds__(kPrepThreads, 1) block_prep_kernel(const PrepArgs p) {
   __shared__ float qs_[kPrepHeads][kHeadDim];
   __shared__ float ks_[kPrepHeads][kHeadDim];
   __shared__ float red[3][kPrepThreads / 32];
   const int h0 = blockIdx.x * kPrepHeads;
-  const int r = blockIdx.y;
-  const int b = r;  // n == 1
+  const int b = blockIdx.y;
   const int t = threadIdx.x;
   const int dq = t / kPrepHeads, hq = t % kPrepHeads;
   const int cq = dq * p.nh + h0 + hq;
@@ -243,8 +259,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1) block_prep_kernel(const PrepA
   const int h = h0 + hl;
   const int cv = h * kHeadDim + d;
   const size_t pstride = (size_t)p.R * p.I;
-  const float* prow = p.Ppart + (size_t)r * p.I;
   const int off_beta = 2 * p.CQ + p.CV + kHeadDim;
+  const int w = t >> 5;
+  const int w0 = hl * (kHeadDim / 32);  // the 4 warps of head hl
 
   // Inputs no earlier kernel of this call writes: fetched before waiting.
   ConvChannel chq, chk, chv;
@@ -257,49 +274,56 @@ __global__ void __launch_bounds__(kPrepThreads, 1) block_prep_kernel(const PrepA
   pdl_wait();
   pdl_trigger();
 
-  float xq = 0.f, xk = 0.f, xv = 0.f, bl = 0.f;
-  for (int ks = 0; ks < p.KS1; ++ks) {
-    const float* pr = prow + ks * pstride;
-    xq += pr[cq];
-    xk += pr[p.CQ + cq];
-    xv += pr[2 * p.CQ + cv];
-    bl += pr[off_beta + h];
-  }
-  const size_t gzrow = (size_t)r * (p.CQ + p.CV);
-  const float graw = p.gz[gzrow + (size_t)h * kHeadDim + d];      // W_fb head-outer
-  const float zz = p.gz[gzrow + p.CQ + (size_t)d * p.nh + h];     // W_gb channel-outer
+#pragma unroll 1
+  for (int j = 0; j < p.n; ++j) {
+    const int r = b * p.n + j;
+    const float* prow = p.Ppart + (size_t)r * p.I;
+    float xq = 0.f, xk = 0.f, xv = 0.f, bl = 0.f;
+    for (int ks = 0; ks < p.KS1; ++ks) {
+      const float* pr = prow + ks * pstride;
+      xq += pr[cq];
+      xk += pr[p.CQ + cq];
+      xv += pr[2 * p.CQ + cv];
+      bl += pr[off_beta + h];
+    }
+    const size_t gzrow = (size_t)r * (p.CQ + p.CV);
+    const float graw = p.gz[gzrow + (size_t)h * kHeadDim + d];      // W_fb head-outer
+    const float zz = p.gz[gzrow + p.CQ + (size_t)d * p.nh + h];     // W_gb channel-outer
 
-  qs_[hq][dq] = conv_apply(p, chq, xq);
-  ks_[hq][dq] = conv_apply(p, chk, xk);
-  const float yv = conv_apply(p, chv, xv);
-  __syncthreads();
-  const float qv = qs_[hl][d], kv = ks_[hl][d];
-  const float qq = warp_sum(qv * qv), kk = warp_sum(kv * kv), qk = warp_sum(qv * kv);
-  const int w = t >> 5;
-  if ((t & 31) == 0) {
-    red[0][w] = qq;
-    red[1][w] = kk;
-    red[2][w] = qk;
-  }
-  __syncthreads();
-  const int w0 = hl * (kHeadDim / 32);  // the 4 warps of head hl
-  float sq = 0.f, sk = 0.f, sqk = 0.f;
+    if (j > 0) __syncthreads();  // the previous token's qs_, ks_ and red are consumed
+    qs_[hq][dq] = conv_step(p, chq, xq);
+    ks_[hq][dq] = conv_step(p, chk, xk);
+    const float yv = conv_step(p, chv, xv);
+    __syncthreads();
+    const float qv = qs_[hl][d], kv = ks_[hl][d];
+    const float qq = warp_sum(qv * qv), kk = warp_sum(kv * kv), qk = warp_sum(qv * kv);
+    if ((t & 31) == 0) {
+      red[0][w] = qq;
+      red[1][w] = kk;
+      red[2][w] = qk;
+    }
+    __syncthreads();
+    float sq = 0.f, sk = 0.f, sqk = 0.f;
 #pragma unroll
-  for (int i = 0; i < kHeadDim / 32; ++i) {
-    sq += red[0][w0 + i];
-    sk += red[1][w0 + i];
-    sqk += red[2][w0 + i];
+    for (int i = 0; i < kHeadDim / 32; ++i) {
+      sq += red[0][w0 + i];
+      sk += red[1][w0 + i];
+      sqk += red[2][w0 + i];
+    }
+    const float qsc = p.scale * rsqrtf(sq + p.l2_eps);
+    const float ksc = rsqrtf(sk + p.l2_eps);
+    const float beta = sigmoidf_(bl);
+    const float g = p.lower_bound * sigmoidf_(aexp * (graw + dtb));
+    TokenStage& st = p.stage[(size_t)r * p.nh + h];
+    const float kh = kv * ksc;
+    st.row[d] = RowCoef{expf(g), kh, qv * qsc, beta * kh};
+    st.v[d] = yv;
+    if (d == 0) st.bqk = beta * sqk * qsc * ksc;
+    p.zgate[((size_t)r * p.nh + h) * kHeadDim + d] = gam * sigmoidf_(zz);
   }
-  const float qsc = p.scale * rsqrtf(sq + p.l2_eps);
-  const float ksc = rsqrtf(sk + p.l2_eps);
-  const float beta = sigmoidf_(bl);
-  const float g = p.lower_bound * sigmoidf_(aexp * (graw + dtb));
-  TokenStage& st = p.stage[(size_t)r * p.nh + h];
-  const float kh = kv * ksc;
-  st.row[d] = RowCoef{expf(g), kh, qv * qsc, beta * kh};
-  st.v[d] = yv;
-  if (d == 0) st.bqk = beta * sqk * qsc * ksc;
-  p.zgate[((size_t)r * p.nh + h) * kHeadDim + d] = gam * sigmoidf_(zz);
+  conv_save(p, chq);
+  conv_save(p, chk);
+  conv_save(p, chv);
 }
 
 struct RecArgs {
@@ -308,13 +332,17 @@ struct RecArgs {
   float* S;
   __nv_bfloat16* on2;  // [2R, CV] bf16 hi rows then lo rows
   float rms_norm_eps;
-  int R, nh, CV;
+  int R, n, nh, CV;
 };
 
-// 5. one CTA per (request b, head h): the state tile and the staged token
-// vectors are fetched together, one delta-rule step, then the gated output
-// RMSNorm written as bf16 hi/lo for the output projection.
-__global__ void __launch_bounds__(kThreads, 2) block_recurrence_kernel(const RecArgs p) {
+// 5. one CTA per (request b, head h): the state tile is fetched once and held
+// in registers across the request's n tokens; per token the staged vectors
+// are read, one delta-rule step is taken and the gated output RMSNorm is
+// written as bf16 hi/lo for the output projection.
+// kMulti: the n > 1 form (more registers for the token loop, 1 CTA per SM);
+// the n = 1 form keeps 2 CTAs per SM.
+template <bool kMulti>
+__global__ void __launch_bounds__(kThreads, kMulti ? 1 : 2) block_recurrence_kernel(const RecArgs p) {
   __shared__ TokenStage ts;
   __shared__ __align__(16) float zg[kHeadDim];
   __shared__ __align__(16) float o_s[kHeadDim];
@@ -330,24 +358,29 @@ __global__ void __launch_bounds__(kThreads, 2) block_recurrence_kernel(const Rec
   pdl_wait();
   pdl_trigger();
   constexpr int kStageVec = (int)(sizeof(TokenStage) / sizeof(uint4));
-  const uint4* src = reinterpret_cast<const uint4*>(p.stage + bh);
-  for (int i = tid; i < kStageVec; i += kThreads) reinterpret_cast<uint4*>(&ts)[i] = src[i];
-  if (tid < kHeadDim / 4)
-    reinterpret_cast<uint4*>(zg)[tid] =
-        reinterpret_cast<const uint4*>(p.zgate + (size_t)bh * kHeadDim)[tid];
-  __syncthreads();
-  const float4 o = tile_token_step(s, ts, tl);
-  if (tl.rg == 0) *reinterpret_cast<float4*>(&o_s[tl.col]) = o;
-  tile_store(tile, s, tl);
-  __syncthreads();
-  const float od = tid < kHeadDim ? o_s[tid] : 0.f;
-  const float m2 = block_sum(od * od, red);
-  if (tid < kHeadDim) {
-    const float inv = rsqrtf(m2 / (float)kHeadDim + p.rms_norm_eps);
-    const size_t col = (size_t)h * kHeadDim + tid;  // W_o rows are head-outer
-    split_bf16(od * inv * zg[tid], p.on2 + (size_t)b * p.CV + col,
-               p.on2 + ((size_t)p.R + b) * p.CV + col);
+  const int n = kMulti ? p.n : 1;
+#pragma unroll 1
+  for (int j = 0; j < n; ++j) {
+    const size_t r = (size_t)b * n + j;
+    if (j > 0) __syncthreads();  // the previous token's ts, zg and o_s are consumed
+    const uint4* src = reinterpret_cast<const uint4*>(p.stage + r * p.nh + h);
+    for (int i = tid; i < kStageVec; i += kThreads) reinterpret_cast<uint4*>(&ts)[i] = src[i];
+    if (tid < kHeadDim / 4)
+      reinterpret_cast<uint4*>(zg)[tid] =
+          reinterpret_cast<const uint4*>(p.zgate + (r * p.nh + h) * kHeadDim)[tid];
+    __syncthreads();
+    const float4 o = tile_token_step(s, ts, tl);
+    if (tl.rg == 0) *reinterpret_cast<float4*>(&o_s[tl.col]) = o;
+    __syncthreads();
+    const float od = tid < kHeadDim ? o_s[tid] : 0.f;
+    const float m2 = block_sum(od * od, red);
+    if (tid < kHeadDim) {
+      const float inv = rsqrtf(m2 / (float)kHeadDim + p.rms_norm_eps);
+      const size_t col = (size_t)h * kHeadDim + tid;  // W_o rows are head-outer
+      split_bf16(od * inv * zg[tid], p.on2 + r * p.CV + col, p.on2 + ((size_t)p.R + r) * p.CV + col);
+    }
   }
+  tile_store(tile, s, tl);
 }
 
 // 7. out = sum of the split-K partials (float4 granularity).
@@ -415,13 +448,14 @@ cudaError_t launch_kda_block(const BlockArgs& a, cudaStream_t stream) {
   pa.lower_bound = a.lower_bound;
   pa.l2_eps = a.l2_eps;
   pa.R = L.R;
+  pa.n = a.n;
   pa.I = L.I;
   pa.KS1 = L.KS1;
   pa.nh = a.nh;
   pa.Kc = a.Kc;
   pa.CQ = L.CQ;
   pa.CV = L.CV;
-  e = launch(block_prep_kernel, dim3(a.nh / kPrepHeads, L.R), dim3(kPrepThreads), 0, stream, true,
+  e = launch(block_prep_kernel, dim3(a.nh / kPrepHeads, a.B), dim3(kPrepThreads), 0, stream, true,
              pa);
   if (e != cudaSuccess) return e;
   RecArgs ra;
@@ -431,9 +465,11 @@ cudaError_t launch_kda_block(const BlockArgs& a, cudaStream_t stream) {
   ra.on2 = on2;
   ra.rms_norm_eps = a.rms_norm_eps;
   ra.R = L.R;
+  ra.n = a.n;
   ra.nh = a.nh;
   ra.CV = L.CV;
-  e = launch(block_recurrence_kernel, dim3(L.R * a.nh), dim3(kThreads), 0, stream, true, ra);
+  e = launch(a.n > 1 ? block_recurrence_kernel<true> : block_recurrence_kernel<false>,
+             dim3(a.B * a.nh), dim3(kThreads), 0, stream, true, ra);
   if (e != cudaSuccess) return e;
   e = launch_tc_gemm(reinterpret_cast<const kda_bf16*>(on2), L.R, L.CV, a.W_o, a.Hd, L.KS2, opart,
                      err, stream, true);

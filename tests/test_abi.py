@@ -92,7 +92,7 @@ def block_args(**kw):
 
 @pytest.mark.parametrize("kw,expect", [
     ({"B": -1}, ERR_SHAPE), ({"n": 0}, ERR_SHAPE), ({"Kc": 0}, ERR_SHAPE),
-    ({"n": 2}, ERR_UNSUP), ({"K": 64}, ERR_UNSUP), ({"Kc": 5}, ERR_UNSUP),
+    ({"K": 64}, ERR_UNSUP), ({"Kc": 5}, ERR_UNSUP),
     ({"Hd": 4000}, ERR_UNSUP), ({"nh": 12}, ERR_UNSUP),
     ({"lower_bound": 1.0}, ERR_VALUE), ({"scale": float("inf")}, ERR_VALUE),
     ({"rms_norm_eps": -1.0}, ERR_VALUE),
@@ -109,7 +109,8 @@ def test_block_workspace_size(lib):
     ws = lib.kda_block_tkg_workspace_size(32, 1, 4096, 32, 128, 128, 4)
     assert ws > 0 and ws % 256 == 0
     assert lib.kda_block_tkg_workspace_size(64, 1, 4096, 32, 128, 128, 4) > ws
-    assert lib.kda_block_tkg_workspace_size(32, 2, 4096, 32, 128, 128, 4) == 0
+    assert lib.kda_block_tkg_workspace_size(32, 2, 4096, 32, 128, 128, 4) > ws   # R = B * n rows
+    assert lib.kda_block_tkg_workspace_size(32, 0, 4096, 32, 128, 128, 4) == 0
     assert lib.kda_block_tkg_workspace_size(32, 1, 4096, 12, 128, 128, 4) == 0
 
 
