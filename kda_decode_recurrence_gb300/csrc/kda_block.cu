@@ -9,7 +9,8 @@
 // Kernel chain on the caller's stream (rows r = b * n + j for token j of request
 // b, R = B * n):
 //   1. rmsnorm      x = hidden * rsqrt(mean(hidden^2) + eps) * gamma_in, written
-//                   as bf16 hi/lo halves X2 [2R, Hd] for the tensor cores
+//                   as bf16 hi/lo halves X2 [2R, Hd] for the tensor cores; out
+//                   zeroed
 //   2. proj GEMM    tcgen05, P_part[ks] = x[:, split ks] . W_in[split ks, :]   [KS1, R, I]
 //                   (split-K so every SM streams a slice of the 103 MB W_in;
 //                   consumers add the KS1 partial sums)
@@ -22,8 +23,8 @@
 //   5. recurrence   one CTA per (b, h): the register-tile delta-rule step on
 //                   S[b, h] (shared with kda_decode), gated output RMSNorm ->
 //                   bf16 hi/lo on2
-//   6. out GEMM     tcgen05, O_part[ks] = on[:, split ks] . W_o[split ks, :]   [KS2, R, Hd]
-//   7. reduce       out = sum_ks O_part[ks]
+//   6. out GEMM     tcgen05, out += on[:, split ks] . W_o[split ks, :] for each
+//                   split (fp32 atomics into the rows the RMSNorm kernel zeroed)
 // Intermediates live in the caller's workspace (a few MB: L2-resident).
 #include "kda_recurrence.cuh"
 #include "kda_launch.h"
@@ -35,12 +36,12 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kLatCols = 64;   // latent GEMM: output columns per CTA
 constexpr int kLatRows = 32;   // latent GEMM: rows per CTA
-constexpr int kKS1 = 4;        // contraction splits of the W_in GEMM
-constexpr int kKS2 = 8;        // contraction splits of the W_o GEMM
+constexpr int kKS1 = 3;        // contraction splits of the W_in GEMM (99 tiles x 3 = 297 CTAs: one wave at 2 per SM)
+constexpr int kKS2 = 9;        // contraction splits of the W_o GEMM (32 tiles x 9 = 288 CTAs)
 
 struct Layout {
   int R, I, CQ, CV, KS1, KS2;
-  size_t x2, ppart, gz, stage, zgate, on2, opart, err, total;
+  size_t x2, ppart, gz, stage, zgate, on2, err, total;
 };
 
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -62,7 +63,6 @@ bool make_layout(int B, int n, int Hd, int nh, int K, int V, int Kc, Layout* L) 
   L->stage = off; off = align_up(off + sizeof(TokenStage) * (size_t)L->R * nh);
   L->zgate = off; off = align_up(off + sizeof(float) * (size_t)L->R * L->CV);
   L->on2 = off;   off = align_up(off + 2 * sizeof(kda_bf16) * (size_t)L->R * L->CV);
-  L->opart = off; off = align_up(off + sizeof(float) * (size_t)L->KS2 * L->R * Hd);
   L->err = off;   off = align_up(off + sizeof(int32_t));
   L->total = off;
   return true;
@@ -87,24 +87,55 @@ __device__ __forceinline__ float block_sum(float x, float* red /* [kThreads/32] 
   return t;
 }
 
-// 1. input RMSNorm, one CTA per row, written as bf16 hi/lo halves.
-__global__ void __launch_bounds__(kThreads) rmsnorm_split_kernel(const float* __restrict__ hidden,
-                                                                 const float* __restrict__ gamma,
-                                                                 __nv_bfloat16* __restrict__ X2,
-                                                                 int R, int Hd, float eps) {
-  __shared__ float red[kThreads / 32];
+constexpr int kNormThreads = 1024;
+constexpr int kNormCache = 4;  // float4 per thread held in registers (Hd <= 16384)
+
+// 1. input RMSNorm, one CTA per row: the row is read once into registers,
+// reduced, and written as bf16 hi/lo halves.  The CTA also zeroes its row of
+// `out`, which the output projection accumulates into.
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_split_kernel(
+    const float* __restrict__ hidden, const float* __restrict__ gamma,
+    __nv_bfloat16* __restrict__ X2, float* __restrict__ out, int R, int Hd, float eps) {
+  __shared__ float red[kNormThreads / 32];
   pdl_trigger();
   const float* x = hidden + (size_t)blockIdx.x * Hd;
+  float4 xv[kNormCache];
   float ss = 0.f;
-  for (int i = threadIdx.x * 4; i < Hd; i += kThreads * 4) {
+#pragma unroll
+  for (int c = 0; c < kNormCache; ++c) {
+    const int i = (threadIdx.x + c * kNormThreads) * 4;
+    xv[c] = i < Hd ? *reinterpret_cast<const float4*>(x + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    ss += xv[c].x * xv[c].x + xv[c].y * xv[c].y + xv[c].z * xv[c].z + xv[c].w * xv[c].w;
+  }
+  for (int i = (threadIdx.x + kNormCache * kNormThreads) * 4; i < Hd; i += kNormThreads * 4) {
     const float4 v = *reinterpret_cast<const float4*>(x + i);
     ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
   }
-  ss = block_sum(ss, red);
-  const float inv = rsqrtf(ss / (float)Hd + eps);
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < kNormThreads / 32; ++w) tot += red[w];
+  const float inv = rsqrtf(tot / (float)Hd + eps);
   __nv_bfloat16* hi = X2 + (size_t)blockIdx.x * Hd;
   __nv_bfloat16* lo = X2 + ((size_t)R + blockIdx.x) * Hd;
-  for (int i = threadIdx.x; i < Hd; i += kThreads) split_bf16(x[i] * inv * gamma[i], hi + i, lo + i);
+  float* orow = out + (size_t)blockIdx.x * Hd;
+  auto emit = [&](int i, float4 v) {
+    const float4 g = *reinterpret_cast<const float4*>(gamma + i);
+    split_bf16(v.x * inv * g.x, hi + i + 0, lo + i + 0);
+    split_bf16(v.y * inv * g.y, hi + i + 1, lo + i + 1);
+    split_bf16(v.z * inv * g.z, hi + i + 2, lo + i + 2);
+    split_bf16(v.w * inv * g.w, hi + i + 3, lo + i + 3);
+    *reinterpret_cast<float4*>(orow + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+  };
+#pragma unroll
+  for (int c = 0; c < kNormCache; ++c) {
+    const int i = (threadIdx.x + c * kNormThreads) * 4;
+    if (i < Hd) emit(i, xv[c]);
+  }
+  for (int i = (threadIdx.x + kNormCache * kNormThreads) * 4; i < Hd; i += kNormThreads * 4)
+    emit(i, *reinterpret_cast<const float4*>(x + i));
 }
 
 // 3. gate latents on the CUDA cores: gz[r][c] = f_a[r] . W_fb[:, c] for
@@ -383,21 +414,6 @@ __global__ void __launch_bounds__(kThreads, kMulti ? 1 : 2) block_recurrence_ker
   tile_store(tile, s, tl);
 }
 
-// 7. out = sum of the split-K partials (float4 granularity).
-__global__ void reduce_partials_kernel(const float* __restrict__ part, int KS, size_t count4,
-                                       float* __restrict__ out) {
-  pdl_wait();
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < count4;
-       i += (size_t)gridDim.x * blockDim.x) {
-    float4 acc = reinterpret_cast<const float4*>(part)[i];
-    for (int ks = 1; ks < KS; ++ks) {
-      const float4 v = reinterpret_cast<const float4*>(part)[(size_t)ks * count4 + i];
-      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-    }
-    reinterpret_cast<float4*>(out)[i] = acc;
-  }
-}
-
 }  // namespace
 
 size_t block_workspace_bytes(int B, int n, int Hd, int nh, int K, int V, int Kc) {
@@ -414,17 +430,16 @@ cudaError_t launch_kda_block(const BlockArgs& a, cudaStream_t stream) {
   float* ppart = reinterpret_cast<float*>(ws + L.ppart);
   float* gz = reinterpret_cast<float*>(ws + L.gz);
   __nv_bfloat16* on2 = reinterpret_cast<__nv_bfloat16*>(ws + L.on2);
-  float* opart = reinterpret_cast<float*>(ws + L.opart);
   int32_t* err = a.dev_status ? a.dev_status : reinterpret_cast<int32_t*>(ws + L.err);
   cudaError_t e;
 
   // The first kernel waits for everything before it in the stream; each later
   // kernel is a programmatic dependent of the one before it.
-  e = launch(rmsnorm_split_kernel, dim3(L.R), dim3(kThreads), 0, stream, false, a.hidden,
-             a.gamma_in, x2, L.R, a.Hd, a.rms_norm_eps);
+  e = launch(rmsnorm_split_kernel, dim3(L.R), dim3(kNormThreads), 0, stream, false, a.hidden,
+             a.gamma_in, x2, a.out, L.R, a.Hd, a.rms_norm_eps);
   if (e != cudaSuccess) return e;
   e = launch_tc_gemm(reinterpret_cast<const kda_bf16*>(x2), L.R, a.Hd, a.W_in, L.I, L.KS1, ppart,
-                     err, stream, true);
+                     false, err, stream, true);
   if (e != cudaSuccess) return e;
   const int off_ga = 2 * L.CQ + L.CV;
   const int off_fa = off_ga + kHeadDim + a.nh;
@@ -471,13 +486,10 @@ cudaError_t launch_kda_block(const BlockArgs& a, cudaStream_t stream) {
   e = launch(a.n > 1 ? block_recurrence_kernel<true> : block_recurrence_kernel<false>,
              dim3(a.B * a.nh), dim3(kThreads), 0, stream, true, ra);
   if (e != cudaSuccess) return e;
-  e = launch_tc_gemm(reinterpret_cast<const kda_bf16*>(on2), L.R, L.CV, a.W_o, a.Hd, L.KS2, opart,
-                     err, stream, true);
-  if (e != cudaSuccess) return e;
-  const size_t count4 = (size_t)L.R * a.Hd / 4;
-  const int rblk = (int)((count4 + kThreads - 1) / kThreads);
-  return launch(reduce_partials_kernel, dim3(rblk), dim3(kThreads), 0, stream, true,
-                (const float*)opart, L.KS2, count4, a.out);
+  // The output projection adds its contraction splits straight into `out`
+  // (zeroed by the RMSNorm kernel).
+  return launch_tc_gemm(reinterpret_cast<const kda_bf16*>(on2), L.R, L.CV, a.W_o, a.Hd, L.KS2,
+                        a.out, true, err, stream, true);
 }
 
 }  // namespace kda

@@ -104,10 +104,11 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 
 struct GemmShape {
-  int R;       // tokens
-  int Kdim;    // contraction length (multiple of 64)
-  int N;       // output columns (multiple of 8)
-  int KS;      // contraction splits
+  int R;           // tokens
+  int Kdim;        // contraction length (multiple of 64)
+  int N;           // output columns (multiple of 8)
+  int KS;          // contraction splits
+  int accumulate;  // add each split into Y[r][n] instead of writing Ypart[ks]
 };
 
 // Dynamic shared memory: kStages x (A 16 KiB + B 2*RB*128 B), 1024-aligned,
@@ -234,7 +235,12 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int r = r0 + c * 32 + j;
-          if (r < sh.R) Ypart[((size_t)ks * sh.R + r) * sh.N + m] = hi[j] + lo[j];
+          if (r < sh.R) {
+            if (sh.accumulate)
+              atomicAdd(Ypart + (size_t)r * sh.N + m, hi[j] + lo[j]);
+            else
+              Ypart[((size_t)ks * sh.R + r) * sh.N + m] = hi[j] + lo[j];
+          }
         }
       }
     }
@@ -291,7 +297,8 @@ size_t tc_gemm_smem_bytes(int R) {
 }
 
 cudaError_t launch_tc_gemm(const kda_bf16* X2, int R, int Kdim, const kda_bf16* W, int N, int KS,
-                           float* Ypart, int32_t* err, cudaStream_t stream, bool pdl) {
+                           float* Ypart, bool accumulate, int32_t* err, cudaStream_t stream,
+                           bool pdl) {
   if (R < 1 || Kdim % kBK != 0 || N % 8 != 0 || KS < 1 || KS > Kdim / kBK)
     return cudaErrorInvalidValue;
   CUtensorMap tmW, tmX;
@@ -301,7 +308,7 @@ cudaError_t launch_tc_gemm(const kda_bf16* X2, int R, int Kdim, const kda_bf16* 
   cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  GemmShape sh{R, Kdim, N, KS};
+  GemmShape sh{R, Kdim, N, KS, accumulate ? 1 : 0};
   dim3 grid((N + kTileN - 1) / kTileN, KS, (R + 127) / 128);
   return launch(tc_gemm_kernel, grid, dim3(128), smem, stream, pdl, tmW, tmX, Ypart, sh, err);
 }

@@ -9,7 +9,9 @@
 
 namespace kda {
 
-// Ypart[ks][r][n] = sum over contraction split ks of (X2[r][k] + X2[R + r][k]) * W[k][n].
+// Ypart[ks][r][n] = sum over contraction split ks of (X2[r][k] + X2[R + r][k]) * W[k][n],
+// or, with `accumulate`, every split added into Ypart[r][n] (fp32 atomics;
+// Ypart [R, N] must hold the starting value, e.g. zeros).
 // X2 bf16 [2R, Kdim] (hi rows then lo rows), W bf16 [Kdim, N] (row k contiguous),
 // Ypart fp32 [KS, R, N].  Kdim % 64 == 0, N % 8 == 0, 1 <= KS <= Kdim / 64,
 // 16-byte aligned pointers.  On an internal pipeline timeout the kernel ORs
@@ -17,7 +19,8 @@ namespace kda {
 // the kernel is a programmatic dependent of the previous kernel in the stream
 // (it requests its first weight tiles before waiting for that kernel).
 cudaError_t launch_tc_gemm(const kda_bf16* X2, int R, int Kdim, const kda_bf16* W, int N, int KS,
-                           float* Ypart, int32_t* err, cudaStream_t stream, bool pdl);
+                           float* Ypart, bool accumulate, int32_t* err, cudaStream_t stream,
+                           bool pdl);
 
 size_t tc_gemm_smem_bytes(int R);
 

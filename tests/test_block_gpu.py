@@ -7,7 +7,7 @@ import oracle
 from kda_decode_recurrence_gb300 import block_workspace_size, kda_block_tkg
 from kda_decode_recurrence_gb300.inputs import block_inputs, to_f64
 
-from _parity import assert_outputs_close, assert_states_close, to_device
+from _parity import STATE_RTOL, assert_outputs_close, assert_states_close, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -34,7 +34,11 @@ def check_block(inp):
     out, S, cs = gpu_block(inp)
     ref_out, ref_S, ref_cs = oracle_block(inp)
     assert_outputs_close(out.cpu().numpy(), ref_out, "out")
-    assert_states_close(S.cpu().numpy(), ref_S, "S")
+    # Each token multiplies S by decay factors exp(g) whose fp32 rounding the
+    # gate amplifies (|dg/dgraw| <= |lower_bound| * exp(A_log) / 4 = 20 here),
+    # so the relative state error grows with the tokens chained in one call:
+    # the 1e-5 bound holds per token, n * 1e-5 for n tokens.
+    assert_states_close(S.cpu().numpy(), ref_S, "S", tol=STATE_RTOL * inp["n"])
     # conv_state: the last Kc-1 pre-convolution inputs.  With one token the
     # older entries are exact copies shifted by one; entries that come from
     # this call's projection carry the GEMM's rounding.
@@ -59,7 +63,9 @@ def test_block_workspace_reuse_is_stateless():
                     device="cuda")
     out1, _, _ = gpu_block(inp, ws)
     out2, _, _ = gpu_block(inp, ws)       # stale workspace contents must not matter
-    assert torch.equal(out1, out2)
+    # the output projection adds its contraction splits with fp32 atomics, so
+    # repeated calls agree to rounding, not bit for bit
+    assert_outputs_close(out2.cpu().numpy(), out1.cpu().double().numpy(), "repeat")
 
 
 # -------------------------------------------- n > 1 tokens per request
