@@ -368,6 +368,46 @@ def run_decode_variant(inp: dict, d: dict, steps: int) -> dict:
             "peak_source": src, "state_updates_per_s": T * HV / t}
 
 
+def prefill_flops(T: int, HV: int, K: int, V: int) -> int:
+    """fp32 flops of the recurrence over T tokens of HV heads: per token and
+    head the decay (K*V), k^T S (2 K V), the rank-1 write (2 K V) and the read
+    (2 K V)."""
+    return T * HV * 7 * K * V
+
+
+def run_prefill(steps: int, warmup: int, impl: str = "recurrent") -> dict:
+    """Whole-prompt prefill: B = 2 requests x 2048 tokens, H = HV = 96,
+    lower-bound gate, state from the pool, final state written back."""
+    from kda_decode_recurrence_gb300 import kda_decode
+    B, L = 2, 2048
+    inp = decode_inputs(DECODE_CONFIGS["varlen"], B=B, H=96, HV=96, max_slots=4,
+                        lengths=(L,) * B, seed=7)
+    dev = torch.device("cuda", 0)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    out = torch.empty(inp["T"], inp["HV"], inp["V"], device=dev)
+
+    def call():
+        kda_decode(out, d["q"], d["k"], d["v"], d["raw_gate"], d["beta_logits"], d["a_log"],
+                   d["dt_bias"], d["cu_seqlens"], d["state_pool"], d["state_indices"],
+                   gate_mode=inp["gate_mode"], lower_bound=inp["lower_bound"])
+
+    for _ in range(warmup):
+        call()
+    times = []
+    for _ in range(steps):
+        s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_.record()
+        call()
+        e_.record()
+        e_.synchronize()
+        times.append(s_.elapsed_time(e_) * 1e-3)
+    t = statistics.median(times)
+    fl = prefill_flops(inp["T"], inp["HV"], inp["K"], inp["V"])
+    return {"impl": impl, "workload": f"prefill B={B} x {L} tokens, H=HV=96, lower-bound gate",
+            "ms": t * 1e3, "tokens_per_s": inp["T"] / t, "state_updates_per_s": inp["T"] * inp["HV"] / t,
+            "tflops": fl / t / 1e12}
+
+
 def run_gpu(args, rank, world, local):
     from kda_decode_recurrence_gb300 import kda_decode
     cfg = DECODE_CONFIGS[WORKLOAD]
@@ -498,6 +538,9 @@ def run_profile_case(args, which: str):
     if which == "block":
         print(json.dumps({"profile": "block", **run_block(args.steps, args.warmup)}))
         return
+    if which == "prefill":
+        print(json.dumps({"profile": "prefill", **run_prefill(args.steps, args.warmup)}))
+        return
     inp = decode_inputs(DECODE_CONFIGS[WORKLOAD], B=32, max_slots=64)
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     out = torch.empty(inp["T"], inp["HV"], inp["V"], device=dev)
@@ -520,7 +563,7 @@ def run_profile_case(args, which: str):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile", choices=["decode", "block"], default=None,
+    ap.add_argument("--profile", choices=["decode", "block", "prefill"], default=None,
                     help="run a reduced case of one kernel for ncu (no JSON bench line)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)

@@ -20,9 +20,10 @@
 //     rows rg, rg + 8, ..., rg + 120 of its four columns (16 float4);
 //   * the k- and q-contractions over the 128 key rows are in-thread sums over
 //     16 rows followed by three xor-shuffles across the 8 row groups;
-//   * each warp prepares its own copy of the token's vectors (normalised q
-//     and k, exp(g), beta * k, v, beta * q.k) in a private shared-memory
-//     record, so warps never wait for each other inside an item;
+//   * each warp prepares its own copy of the first token's vectors (normalised
+//     q and k, exp(g), beta * k, v, beta * q.k) in a private shared-memory
+//     record while the tile is in flight; later tokens of an item are staged
+//     8 at a time, one warp per token, between two CTA barriers;
 //   * the advanced tile is written back from registers with 128-bit
 //     streaming stores.
 //
@@ -158,9 +159,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_kernel(const DecodeArg
   Item* descs = reinterpret_cast<Item*>(wstage + kWarps);
   uint64_t* bars = reinterpret_cast<uint64_t*>(descs + kBufs);
 
+  const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const TileLane tl = tile_lane();
-  TokenStage& ts = wstage[threadIdx.x >> 5];
+  TokenStage& ts = wstage[warp];
   const long long items = (long long)p.B * p.HV;
   const long long G = gridDim.x;
   const long long first = blockIdx.x;
@@ -234,18 +236,28 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_kernel(const DecodeArg
     }
     if (!tile) continue;  // no tokens: the state stays bit-identical
 
-    TokenIn nxt = {};
-    if (d.t0 + 1 < d.t1) nxt = fetch_token(p, d.t0 + 1, h, d.hv, lane);
-    for (int t = d.t0; t < d.t1; ++t) {
-      if (t != d.t0) {
-        __syncwarp();  // every lane is done with the previous token's record
-        build_stage(p, nxt, ts, lane);
-        if (t + 1 < d.t1) nxt = fetch_token(p, t + 1, h, d.hv, lane);
-      }
-      __syncwarp();
+    // First token: this warp's own record, built while the tile was in flight.
+    __syncwarp();
+    {
       const float4 o = tile_token_step(s, ts, tl);
-      if (tl.rg == 0) store_out<kOutBf16>(p, t, d.hv, tl.col, o);
+      if (tl.rg == 0) store_out<kOutBf16>(p, d.t0, d.hv, tl.col, o);
     }
+    // Later tokens, 8 per round: warp w stages token c0 + w into record w, then
+    // every warp steps through the round's records.  (Uniform across the CTA:
+    // every thread handles the same item.)
+    for (int c0 = d.t0 + 1; c0 < d.t1; c0 += kWarps) {
+      const int nc = min(kWarps, d.t1 - c0);
+      __syncthreads();  // all warps are done with the records of the last round
+      if (warp < nc) build_stage(p, fetch_token(p, c0 + warp, h, d.hv, lane), wstage[warp], lane);
+      __syncthreads();
+      for (int jj = 0; jj < nc; ++jj) {
+        const float4 o = tile_token_step(s, wstage[jj], tl);
+        if (tl.rg == 0) store_out<kOutBf16>(p, c0 + jj, d.hv, tl.col, o);
+      }
+    }
+    // The next item's first record goes into wstage[warp]: wait until every
+    // warp has finished reading this item's rounds.
+    if (d.t1 - d.t0 > 1) __syncthreads();
     float* dst = tile_ptr(p, d);
     if (kVFirst) {
       // Each instruction writes 4 runs of 8 consecutive floats (full sectors).
