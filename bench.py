@@ -375,10 +375,19 @@ def prefill_flops(T: int, HV: int, K: int, V: int) -> int:
     return T * HV * 7 * K * V
 
 
-def run_prefill(steps: int, warmup: int, impl: str = "recurrent") -> dict:
+def run_prefill(steps: int, warmup: int) -> dict:
     """Whole-prompt prefill: B = 2 requests x 2048 tokens, H = HV = 96,
-    lower-bound gate, state from the pool, final state written back."""
-    from kda_decode_recurrence_gb300 import kda_decode
+    lower-bound gate, state from the pool, final state written back; timed
+    for the chunked kda_prefill and for kda_decode's token-by-token kernel."""
+    res = {"chunked": _prefill_once(steps, warmup, "chunked"),
+           "recurrent": _prefill_once(steps, warmup, "recurrent")}
+    res["speedup_chunked_vs_recurrent"] = res["recurrent"]["ms"] / res["chunked"]["ms"]
+    return res
+
+
+def _prefill_once(steps: int, warmup: int, impl: str) -> dict:
+    from kda_decode_recurrence_gb300 import kda_decode, kda_prefill
+    fn = kda_prefill if impl == "chunked" else kda_decode
     B, L = 2, 2048
     inp = decode_inputs(DECODE_CONFIGS["varlen"], B=B, H=96, HV=96, max_slots=4,
                         lengths=(L,) * B, seed=7)
@@ -387,9 +396,9 @@ def run_prefill(steps: int, warmup: int, impl: str = "recurrent") -> dict:
     out = torch.empty(inp["T"], inp["HV"], inp["V"], device=dev)
 
     def call():
-        kda_decode(out, d["q"], d["k"], d["v"], d["raw_gate"], d["beta_logits"], d["a_log"],
-                   d["dt_bias"], d["cu_seqlens"], d["state_pool"], d["state_indices"],
-                   gate_mode=inp["gate_mode"], lower_bound=inp["lower_bound"])
+        fn(out, d["q"], d["k"], d["v"], d["raw_gate"], d["beta_logits"], d["a_log"],
+           d["dt_bias"], d["cu_seqlens"], d["state_pool"], d["state_indices"],
+           gate_mode=inp["gate_mode"], lower_bound=inp["lower_bound"])
 
     for _ in range(warmup):
         call()
@@ -490,6 +499,7 @@ def run_gpu(args, rank, world, local):
     block = run_block(steps=max(5, min(args.steps, 50)), warmup=3) if rank == 0 else None
     block_n4 = run_block(steps=max(5, min(args.steps, 50)), warmup=3, n=4) if rank == 0 else None
     variant = run_decode_variant(inp, d, steps=max(5, min(args.steps, 200))) if rank == 0 else None
+    prefill = run_prefill(steps=3, warmup=1) if rank == 0 else None
 
     if rank != 0:
         return
@@ -524,6 +534,7 @@ def run_gpu(args, rank, world, local):
         "block_tkg": block,
         "block_tkg_n4": block_n4,
         "decode_v_first_bf16": variant,
+        "prefill": prefill,
     }
     print(json.dumps(line), flush=True)
 

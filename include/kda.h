@@ -157,6 +157,28 @@ kda_status kda_decode_ex(void* output, const kda_bf16* q, const kda_bf16* k, con
                          int V, int max_slots, int32_t* dev_status, void* stream);
 
 /*
+ * kda_prefill -- the same recurrence as kda_decode, computed in chunks of 16
+ * tokens: the whole-sequence form ("Delta-rule write": the model runs
+ * chunk_kda over a full sequence and fused_recurrent_kda for one new token
+ * with a cache).  Arguments, layouts, outputs, state handling and device
+ * status bits are those of kda_decode (K_FIRST state, fp32 output); the
+ * result equals the token-by-token recurrence up to fp32 rounding.  Meant for
+ * long prompts: each request's tokens are processed 16 at a time by one CTA
+ * per (request, value head).
+ *
+ * Requires gate_mode == KDA_GATE_LOWER_BOUND with -5 <= lower_bound <= 0
+ * ("KDA Block TKG Kernel API Reference", :param lower_bound:, the bound on
+ * the cumulative decay that the chunkwise prefill depends on); otherwise it
+ * returns KDA_ERR_UNSUPPORTED (use kda_decode).
+ */
+kda_status kda_prefill(float* output, const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
+                       const float* raw_gate, const float* beta_logits, const float* a_log,
+                       const float* dt_bias, const int32_t* cu_seqlens, float* state_pool,
+                       const int32_t* state_indices, int gate_mode, float lower_bound, int B,
+                       int T, int H, int HV, int K, int V, int max_slots, int32_t* dev_status,
+                       void* stream);
+
+/*
  * kda_block_tkg -- the fused KDA block for token generation.
  *
  * Defined by "KDA Block TKG Kernel API Reference" (Background; signature;

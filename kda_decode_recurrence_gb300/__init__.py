@@ -92,6 +92,41 @@ def kda_decode(output, q, k, v, raw_gate, beta_logits, a_log, dt_bias, cu_seqlen
     return rc
 
 
+def kda_prefill(output, q, k, v, raw_gate, beta_logits, a_log, dt_bias, cu_seqlens, state_pool,
+                state_indices, gate_mode=GATE_LOWER_BOUND, lower_bound=-5.0, dev_status=None,
+                stream=None, check=True) -> int:
+    """Whole-prompt prefill: the kda_decode recurrence computed 16 tokens at a
+    time (lower-bound gate with lower_bound >= -5 only).  Same tensors as
+    kda_decode."""
+    dev = state_pool.device
+    T = q.shape[-3]
+    H, K = q.shape[-2], q.shape[-1]
+    HV, V = v.shape[-2], v.shape[-1]
+    B = state_indices.shape[0]
+    N = state_pool.shape[0]
+    for t, n, dt in ((output, "output", torch.float32), (q, "q", torch.bfloat16),
+                     (k, "k", torch.bfloat16), (v, "v", torch.bfloat16),
+                     (raw_gate, "raw_gate", torch.float32),
+                     (beta_logits, "beta_logits", torch.float32), (a_log, "a_log", torch.float32),
+                     (dt_bias, "dt_bias", torch.float32), (cu_seqlens, "cu_seqlens", torch.int32),
+                     (state_pool, "state_pool", torch.float32),
+                     (state_indices, "state_indices", torch.int32)):
+        _check(t, n, dt, dev)
+    if tuple(state_pool.shape[1:]) != (HV, K, V):
+        raise ValueError(f"state_pool shape {tuple(state_pool.shape)} != [N, {HV}, {K}, {V}]")
+    if cu_seqlens.numel() != B + 1:
+        raise ValueError("cu_seqlens must have B + 1 entries")
+    rc = _lib.load().kda_prefill(
+        output.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), raw_gate.data_ptr(),
+        beta_logits.data_ptr(), a_log.data_ptr(), dt_bias.data_ptr(), cu_seqlens.data_ptr(),
+        state_pool.data_ptr(), state_indices.data_ptr(), int(gate_mode), float(lower_bound),
+        B, T, H, HV, K, V, N, None if dev_status is None else dev_status.data_ptr(),
+        _stream_handle(stream))
+    if check and rc != 0:
+        raise KdaError(rc, "kda_prefill")
+    return rc
+
+
 def kda_decode_ex(output, q, k, v, raw_gate, beta_logits, a_log, dt_bias, cu_seqlens, state_pool,
                   state_indices, gate_mode=GATE_SOFTPLUS, lower_bound=-5.0,
                   state_layout=STATE_K_FIRST, dev_status=None, stream=None, check=True) -> int:

@@ -14,7 +14,7 @@ _lock = threading.Lock()
 _lib = None
 
 # Every symbol include/kda.h declares.
-EXPORTS = ("kda_decode", "kda_decode_ex", "kda_block_tkg", "kda_block_tkg_static",
+EXPORTS = ("kda_decode", "kda_decode_ex", "kda_prefill", "kda_block_tkg", "kda_block_tkg_static",
            "kda_block_tkg_workspace_size", "kda_status_string", "kda_version")
 
 STATUS = {
@@ -28,6 +28,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.kda_decode.restype = i
     lib.kda_decode.argtypes = [vp] * 11 + [i, f] + [i] * 7 + [vp, vp]
+    lib.kda_prefill.restype = i
+    lib.kda_prefill.argtypes = [vp] * 11 + [i, f] + [i] * 7 + [vp, vp]
     lib.kda_decode_ex.restype = i
     lib.kda_decode_ex.argtypes = [vp] * 11 + [i, f, i, i] + [i] * 7 + [vp, vp]
     lib.kda_block_tkg.restype = i

@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libkda.so")
 
-SOURCES = ["kda_api.cu", "kda_decode.cu", "kda_block.cu", "kda_tc_gemm.cu", "kda_block_static.cu"]
+SOURCES = ["kda_api.cu", "kda_decode.cu", "kda_block.cu", "kda_tc_gemm.cu", "kda_block_static.cu", "kda_prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
               "--expt-relaxed-constexpr"]

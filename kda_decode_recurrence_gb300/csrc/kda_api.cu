@@ -40,7 +40,8 @@ kda_status decode_impl(void* output, const kda_bf16* q, const kda_bf16* k, const
                        const float* dt_bias, const int32_t* cu_seqlens, float* state_pool,
                        const int32_t* state_indices, int gate_mode, float lower_bound,
                        int state_layout, int output_dtype, int B, int T, int H, int HV, int K,
-                       int V, int max_slots, int32_t* dev_status, void* stream) {
+                       int V, int max_slots, int32_t* dev_status, void* stream,
+                       bool prefill = false) {
   if (B < 0 || T < 0 || H < 1 || HV < 1 || K < 1 || V < 1 || max_slots < 1) return KDA_ERR_SHAPE;
   if (HV % H != 0) return KDA_ERR_SHAPE;
   if (gate_mode != KDA_GATE_SOFTPLUS && gate_mode != KDA_GATE_LOWER_BOUND) return KDA_ERR_ENUM;
@@ -85,9 +86,9 @@ kda_status decode_impl(void* output, const kda_bf16* q, const kda_bf16* k, const
   a.HV = HV;
   a.G = HV / H;
   a.max_slots = max_slots;
-  if (kda::launch_kda_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return KDA_ERR_CUDA;
-  return KDA_OK;
+  const cudaError_t e = prefill ? kda::launch_kda_prefill(a, static_cast<cudaStream_t>(stream))
+                                : kda::launch_kda_decode(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 }  // namespace
@@ -114,6 +115,20 @@ kda_status kda_decode_ex(void* output, const kda_bf16* q, const kda_bf16* k, con
   return decode_impl(output, q, k, v, raw_gate, beta_logits, a_log, dt_bias, cu_seqlens,
                      state_pool, state_indices, gate_mode, lower_bound, state_layout,
                      output_dtype, B, T, H, HV, K, V, max_slots, dev_status, stream);
+}
+
+kda_status kda_prefill(float* output, const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
+                       const float* raw_gate, const float* beta_logits, const float* a_log,
+                       const float* dt_bias, const int32_t* cu_seqlens, float* state_pool,
+                       const int32_t* state_indices, int gate_mode, float lower_bound, int B,
+                       int T, int H, int HV, int K, int V, int max_slots, int32_t* dev_status,
+                       void* stream) {
+  if (gate_mode == KDA_GATE_SOFTPLUS) return KDA_ERR_UNSUPPORTED;  // unbounded decay
+  if (gate_mode == KDA_GATE_LOWER_BOUND && std::isfinite(lower_bound) && lower_bound < -5.0f)
+    return KDA_ERR_UNSUPPORTED;
+  return decode_impl(output, q, k, v, raw_gate, beta_logits, a_log, dt_bias, cu_seqlens,
+                     state_pool, state_indices, gate_mode, lower_bound, KDA_STATE_K_FIRST,
+                     KDA_OUTPUT_F32, B, T, H, HV, K, V, max_slots, dev_status, stream, true);
 }
 
 size_t kda_block_tkg_workspace_size(int B, int n, int Hd, int nh, int K, int V, int Kc) {

@@ -36,6 +36,7 @@ struct DecodeArgs {
 };
 
 cudaError_t launch_kda_decode(const DecodeArgs& args, cudaStream_t stream);
+cudaError_t launch_kda_prefill(const DecodeArgs& args, cudaStream_t stream);
 
 struct BlockArgs {
   float* out;

@@ -130,3 +130,14 @@ def decode_ex_args(**kw):
 ])
 def test_decode_ex_host_validation(lib, kw, expect):
     assert lib.kda_decode_ex(*decode_ex_args(**kw)) == expect
+
+
+@pytest.mark.parametrize("kw,expect", [
+    ({"gate_mode": 0}, ERR_UNSUP),                      # softplus decay is unbounded
+    ({"gate_mode": 1, "lower_bound": -6.0}, ERR_UNSUP),  # |G| over a chunk would exceed 80
+    ({"gate_mode": 1, "lower_bound": 0.5}, ERR_VALUE),
+    ({"gate_mode": 1, "K": 64}, ERR_UNSUP),
+    ({"gate_mode": 1, "B": 0}, KDA_OK),
+])
+def test_prefill_host_validation(lib, kw, expect):
+    assert lib.kda_prefill(*decode_args(**kw)) == expect

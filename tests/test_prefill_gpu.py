@@ -1,0 +1,84 @@
+"""kda_prefill (the chunked whole-sequence form) on the GPU against the
+float64 oracle, and against kda_decode's token-by-token kernel on a full-size
+prompt."""
+import numpy as np
+import pytest
+import torch
+
+from kda_decode_recurrence_gb300 import DEV_BAD_SLOT, kda_decode, kda_prefill
+from kda_decode_recurrence_gb300.inputs import decode_inputs
+
+from _parity import (assert_outputs_close, assert_states_close, oracle_decode_sample,
+                     to_device)
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_prefill(inp, fn=kda_prefill):
+    d = to_device(inp)
+    out = torch.full((inp["T"], inp["HV"], inp["V"]), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fn(out, d["q"], d["k"], d["v"], d["raw_gate"], d["beta_logits"], d["a_log"], d["dt_bias"],
+       d["cu_seqlens"], d["state_pool"], d["state_indices"], gate_mode=inp["gate_mode"],
+       lower_bound=inp["lower_bound"], dev_status=status)
+    torch.cuda.synchronize()
+    return out, d["state_pool"], int(status.item())
+
+
+def check(inp, bs=None, state_tol=1e-5):
+    out, pool, st = gpu_prefill(inp)
+    assert st == 0
+    bs = list(range(inp["B"])) if bs is None else bs
+    rows, slots, ref_out, ref_pool = oracle_decode_sample(inp, bs)
+    assert_outputs_close(out.cpu().numpy()[rows], ref_out)
+    assert_states_close(pool[torch.from_numpy(slots.astype(np.int64)).cuda()].cpu().numpy(),
+                        ref_pool, tol=state_tol)
+
+
+@pytest.mark.parametrize("lb", [-5.0, -1.0])
+def test_chunk_boundaries_against_oracle(lb):
+    # partial chunks, exactly one chunk, one past a chunk, several chunks
+    inp = decode_inputs("varlen", B=6, H=2, HV=4, max_slots=8,
+                        lengths=(1, 15, 16, 17, 40, 100), seed=120)
+    inp["lower_bound"] = lb
+    check(inp)
+
+
+def test_long_sequence_against_oracle():
+    inp = decode_inputs("varlen", B=2, H=4, HV=4, max_slots=3, lengths=(1000, 777), seed=121)
+    check(inp)
+
+
+def test_grouped_heads_against_oracle():
+    inp = decode_inputs("varlen", B=3, H=2, HV=8, max_slots=5, lengths=(33, 64, 5), seed=122)
+    check(inp)
+
+
+def test_matches_token_by_token_kernel_on_a_full_prompt():
+    # the bench's prefill workload: 2 requests x 2048 tokens, 96 heads
+    inp = decode_inputs("varlen", B=2, H=96, HV=96, max_slots=4, lengths=(2048, 2048), seed=7)
+    out_c, pool_c, st_c = gpu_prefill(inp)
+    out_r, pool_r, st_r = gpu_prefill(inp, fn=kda_decode)
+    assert st_c == 0 and st_r == 0
+    assert_outputs_close(out_c.cpu().numpy(), out_r.cpu().double().numpy(), "out")
+    slots = inp["state_indices"].long().cuda()
+    assert_states_close(pool_c[slots].cpu().numpy(), pool_r[slots].cpu().double().numpy(), "S")
+    # and a sample of it against the oracle
+    rows, sl, ref_out, ref_pool = oracle_decode_sample(
+        {**inp, "HV": 96}, [0])
+    assert_outputs_close(out_c.cpu().numpy()[rows], ref_out)
+
+
+def test_padded_and_out_of_range_slots():
+    inp = decode_inputs("varlen", B=4, H=2, HV=2, max_slots=5, lengths=(20, 3, 17, 2), seed=123)
+    inp["state_indices"] = torch.tensor([2, -1, 4, 9], dtype=torch.int32)
+    out, pool, st = gpu_prefill(inp)
+    assert st == DEV_BAD_SLOT
+    cu = inp["cu_seqlens"].numpy()
+    o = out.cpu().numpy()
+    assert np.all(o[cu[1]:cu[2]] == 0.0) and np.all(o[cu[3]:cu[4]] == 0.0)
+    for s in (0, 1, 3):
+        assert torch.equal(pool[s].cpu(), inp["state_pool"][s])
+    rows, slots, ref_out, ref_pool = oracle_decode_sample(inp, [0, 2])
+    assert_outputs_close(o[rows], ref_out)
+    assert_states_close(pool[torch.tensor(slots.astype(np.int64)).cuda()].cpu().numpy(), ref_pool)
