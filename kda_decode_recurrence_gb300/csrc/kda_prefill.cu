@@ -105,20 +105,20 @@ __device__ __forceinline__ void stage(const DecodeArgs& p, const ChunkIn& in, bo
   if (lane == 0) sm.beta[tt] = beta;
 }
 
-// (x_t)^T S0 for the 16 tokens of a chunk, x given as xT[channel][token]:
+// (x_t)^T S0 for tokens t0 .. t0 + 7 of a chunk, x given as xT[channel][token]:
 // in-thread partial sums over the lane's 16 rows, then a butterfly
 // reduce-scatter over the 8 row groups (lane bits 16, 8, 4).  Each lane ends
-// with 2 tokens x 4 columns fully summed and writes them to out[token][col].
-__device__ __forceinline__ void project_chunk(const float4 (&s)[16], const float (*xT)[kTS],
-                                              float (*out)[kHeadDim], TileLane tl, int lane) {
-  float acc[kC][4];
+// with one token x 4 columns fully summed and writes it to out[token][col].
+__device__ __forceinline__ void project8(const float4 (&s)[16], const float (*xT)[kTS], int t0,
+                                         float (*out)[kHeadDim], TileLane tl, int lane) {
+  float acc[8][4];
 #pragma unroll
-  for (int t = 0; t < kC; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+  for (int t = 0; t < 8; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const float* xr = xT[tl.rg + 8 * i];
+    const float* xr = xT[tl.rg + 8 * i] + t0;
 #pragma unroll
-    for (int t4 = 0; t4 < kC; t4 += 4) {
+    for (int t4 = 0; t4 < 8; t4 += 4) {
       const float4 x4 = *reinterpret_cast<const float4*>(xr + t4);
       const float xs[4] = {x4.x, x4.y, x4.z, x4.w};
 #pragma unroll
@@ -131,41 +131,38 @@ __device__ __forceinline__ void project_chunk(const float4 (&s)[16], const float
       }
     }
   }
-  // round m = 16: keep tokens [8, 16) if the bit is set, else [0, 8)
+  // each round keeps the upper half of the remaining tokens where the lane
+  // bit is set and adds the partner's copy of them
   const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4;
-#pragma unroll
-  for (int t = 0; t < 8; ++t)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float send = u16 ? acc[t][j] : acc[t + 8][j];
-      const float keep = u16 ? acc[t + 8][j] : acc[t][j];
-      acc[t][j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-    }
-  // now acc[0..8) holds tokens base16 + (0..8), base16 = u16 ? 8 : 0
 #pragma unroll
   for (int t = 0; t < 4; ++t)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float send = u8 ? acc[t][j] : acc[t + 4][j];
-      const float keep = u8 ? acc[t + 4][j] : acc[t][j];
-      acc[t][j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+      const float send = u16 ? acc[t][j] : acc[t + 4][j];
+      const float keep = u16 ? acc[t + 4][j] : acc[t][j];
+      acc[t][j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
     }
 #pragma unroll
   for (int t = 0; t < 2; ++t)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float send = u4 ? acc[t][j] : acc[t + 2][j];
-      const float keep = u4 ? acc[t + 2][j] : acc[t][j];
-      acc[t][j] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+      const float send = u8 ? acc[t][j] : acc[t + 2][j];
+      const float keep = u8 ? acc[t + 2][j] : acc[t][j];
+      acc[t][j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
     }
-  const int base = (u16 ? 8 : 0) + (u8 ? 4 : 0) + (u4 ? 2 : 0);
 #pragma unroll
-  for (int t = 0; t < 2; ++t)
-    *reinterpret_cast<float4*>(&out[base + t][tl.col]) =
-        make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
+  for (int j = 0; j < 4; ++j) {
+    const float send = u4 ? acc[0][j] : acc[1][j];
+    const float keep = u4 ? acc[1][j] : acc[0][j];
+    acc[0][j] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+  const int t = t0 + (u16 ? 4 : 0) + (u8 ? 2 : 0) + (u4 ? 1 : 0);
+  *reinterpret_cast<float4*>(&out[t][tl.col]) = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) kda_prefill_kernel(const DecodeArgs p) {
+// Two CTAs per SM (128 registers, ~100 KB of shared memory each) so that a
+// batch of (request, head) items twice the SM count runs in one wave.
+__global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeArgs p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   PrefillSmem& sm = *reinterpret_cast<PrefillSmem*>(smem_raw);
 
@@ -202,19 +199,16 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_kernel(const DecodeAr
   const float a_exp = expf(p.a_log[hv]);
   float* out = static_cast<float*>(p.output);
 
-  // Token inputs of the chunk's two slots this warp stages (warp, warp + 8),
-  // fetched one chunk ahead.
-  ChunkIn in0 = {}, in1 = {};
-  if (t0 + warp < t1) in0 = fetch(p, t0 + warp, h, hv, lane);
-  if (t0 + warp + 8 < t1) in1 = fetch(p, t0 + warp + 8, h, hv, lane);
-
   for (int c0 = t0; c0 < t1; c0 += kC) {
     const int nc = min(kC, t1 - c0);
-    // ---- phase 1: stage the chunk's tokens; fetch the next chunk's inputs
-    stage(p, in0, warp < nc, a_exp, sm, warp, lane);
-    stage(p, in1, warp + 8 < nc, a_exp, sm, warp + 8, lane);
-    if (c0 + kC + warp < t1) in0 = fetch(p, c0 + kC + warp, h, hv, lane);
-    if (c0 + kC + warp + 8 < t1) in1 = fetch(p, c0 + kC + warp + 8, h, hv, lane);
+    // ---- phase 1: stage the chunk's tokens, warp w takes slots w and w + 8
+    {
+      ChunkIn in0 = {}, in1 = {};
+      if (warp < nc) in0 = fetch(p, c0 + warp, h, hv, lane);
+      if (warp + 8 < nc) in1 = fetch(p, c0 + warp + 8, h, hv, lane);
+      stage(p, in0, warp < nc, a_exp, sm, warp, lane);
+      stage(p, in1, warp + 8 < nc, a_exp, sm, warp + 8, lane);
+    }
     __syncthreads();
     // ---- phase 2: cumulative decays and the decayed key/query forms.
     // Thread c (and c + 128 for the other half of the tokens) owns channel c.
@@ -256,8 +250,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prefill_kernel(const DecodeAr
       sm.Q[t][s2] = q;  // zero above the diagonal
     }
     // ---- phase 4: (D_t kh_t)^T S0 and (D_t qh_t)^T S0 for the chunk
-    project_chunk(s, sm.ktT, sm.ws, tl, lane);
-    project_chunk(s, sm.qtT, sm.qs, tl, lane);
+    project8(s, sm.ktT, 0, sm.ws, tl, lane);
+    project8(s, sm.ktT, 8, sm.ws, tl, lane);
+    project8(s, sm.qtT, 0, sm.qs, tl, lane);
+    project8(s, sm.qtT, 8, sm.qs, tl, lane);
     __syncthreads();
     // ---- phase 5: the triangular solve for u, one value column per thread
     if (tid < kHeadDim) {
