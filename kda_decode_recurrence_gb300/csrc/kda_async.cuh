@@ -4,6 +4,7 @@
 // KDA_DEV_TIMEOUT.
 #pragma once
 
+#include <cuda.h>
 #include <stdint.h>
 
 namespace kda {
@@ -45,6 +46,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     if (done) return true;
     if (global_ns() - t0 > kWaitLimitNs) return false;
   }
+}
+
+// 2-D tiled TMA load of one box at element coordinates (x, y) into dst.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
 }
 
 // One contiguous global -> shared copy of `bytes` (a multiple of 16, both
