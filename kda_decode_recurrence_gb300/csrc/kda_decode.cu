@@ -6,14 +6,15 @@
 // the request's tokens by decay -> delta write -> read, and written back.
 //
 // GB300 design (HBM-bound: 64 KiB in + 64 KiB out per tile, ~1 flop/byte):
-//   * a persistent grid, one 256-thread CTA per SM; CTA c takes the
-//     (request, value head) work items c, c + G, c + 2G, ... (G = grid size);
+//   * a persistent grid, two 256-thread CTAs per SM (128 registers each, so
+//     16 warps per SM hide each other's latency); CTA c takes the (request,
+//     value head) work items c, c + G, c + 2G, ... (G = grid size);
 //   * each tile is fetched with one 64 KiB bulk copy (cp.async.bulk, the
-//     non-tensor TMA path) into a 3-deep shared-memory ring, so up to three
-//     tiles per SM are in flight while the CTA computes on the current one;
-//     an mbarrier per ring slot carries the copy's byte count, and every
-//     item arrives on its slot (with zero bytes when it has no tile to
-//     fetch) so the ring's phases advance uniformly;
+//     non-tensor TMA path) into the CTA's shared-memory slot as soon as the
+//     previous tile has moved into registers, so the next tile is in flight
+//     while the CTA computes (two per SM); an mbarrier carries the copy's
+//     byte count, and every item arrives on it (with zero bytes when it has
+//     no tile to fetch) so its phases advance uniformly;
 //   * the tile moves from shared memory into registers once and stays there
 //     across all of the request's tokens: warp w owns value columns
 //     [16w, 16w + 16); lane = (row group rg 0..7, column quad cg 0..3) holds
@@ -38,7 +39,8 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kBufs = 3;  // tiles in flight per CTA
+constexpr int kBufs = 1;  // tiles in flight per CTA
+constexpr int kCtasPerSm = 2;
 constexpr uint32_t kTileBytes = kHeadDim * kHeadDim * sizeof(float);
 constexpr float kL2Eps = 1e-6f;
 
@@ -151,7 +153,7 @@ __device__ __forceinline__ void store_out(const DecodeArgs& p, int t, int hv, in
 // transposed state); the register tile is still S[k][v], so the element
 // (k, v) is read from and written to v * 128 + k.
 template <bool kVFirst, bool kOutBf16>
-__global__ void __launch_bounds__(kThreads, 1) kda_decode_kernel(const DecodeArgs p) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const DecodeArgs p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   float* ring = reinterpret_cast<float*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
@@ -179,23 +181,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_decode_kernel(const DecodeArg
   }
   __syncthreads();
 
-  // Inputs of the first token of the next item, fetched one item ahead.
-  TokenIn cur = {};
-  if (nmine > 0 && descs[0].has_tile())
-    cur = fetch_token(p, descs[0].t0, descs[0].hv / p.G, descs[0].hv, lane);
-
   int j = 0;
   for (; j < nmine; ++j) {
     const int buf = j % kBufs;
-    const Item d = descs[buf];
+    const Item d = load_item(p, first + (long long)j * G);
     const bool tile = d.has_tile();
     const int h = d.hv / p.G;
     __syncwarp();  // the warp is done with the previous item's record
-    if (tile) build_stage(p, cur, ts, lane);
-    if (j + 1 < nmine) {
-      const Item dn = descs[(j + 1) % kBufs];
-      if (dn.has_tile()) cur = fetch_token(p, dn.t0, dn.hv / p.G, dn.hv, lane);
-    }
+    if (tile) build_stage(p, fetch_token(p, d.t0, h, d.hv, lane), ts, lane);
 
     const bool arrived = mbar_wait(&bars[buf], (uint32_t)(j / kBufs) & 1u);
     float4 s[16];
@@ -307,7 +300,8 @@ cudaError_t launch_kda_decode(const DecodeArgs& args, cudaStream_t stream) {
                    : (args.out_bf16 ? kda_decode_kernel<false, true> : kda_decode_kernel<false, false>);
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const long long grid = items < sms ? items : sms;
+  const long long slots = (long long)sms * kCtasPerSm;
+  const long long grid = items < slots ? items : slots;
   kernel<<<(unsigned)grid, kThreads, smem, stream>>>(args);
   return cudaGetLastError();
 }
