@@ -46,8 +46,8 @@ FALLBACK_HBM_GBS = 6800.0
 # profiles/), tied to the kernel sources they were taken with: when the
 # sources change the figure no longer describes the kernel and is reported
 # as null.
-NCU_TRAFFIC = {"sources_sha256": "023092f3028d5a9bcb36055bb4a867f88d2046eb79df0f5387f50d3c57c211b3",
-               "bytes_per_launch": 1638365696 + 1576406784}  # read + write, grouped workload
+NCU_TRAFFIC = {"sources_sha256": "b2476a05ff93dbcbc7f78b08555810c61eaa200cf86e0138b4ead9c1982b75aa",
+               "bytes_per_launch": 1638315776 + 1576338176}  # read + write, grouped workload
 
 
 def kernel_sources_sha() -> str:

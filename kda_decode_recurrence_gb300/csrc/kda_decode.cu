@@ -122,12 +122,10 @@ __device__ __forceinline__ float* tile_ptr(const DecodeArgs& p, const Item& d) {
   return p.state_pool + ((size_t)d.slot * p.HV + d.hv) * (size_t)(kHeadDim * kHeadDim);
 }
 
-// Arrive on the ring slot for `item`, start its tile copy when it has one,
-// and leave its descriptor beside the slot for the other threads.
+// Arrive on the ring slot for `item` and start its tile copy when it has one.
 __device__ __forceinline__ void issue_item(const DecodeArgs& p, long long item, float* dst,
-                                           uint64_t* bar, Item* desc) {
+                                           uint64_t* bar) {
   const Item d = load_item(p, item);
-  *desc = d;
   const bool copy = d.has_tile();
   mbar_expect_tx(bar, copy ? kTileBytes : 0u);
   if (copy) bulk_load(dst, tile_ptr(p, d), kTileBytes, bar);
@@ -158,8 +156,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
   float* ring = reinterpret_cast<float*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   TokenStage* wstage = reinterpret_cast<TokenStage*>(ring + kBufs * kHeadDim * kHeadDim);
-  Item* descs = reinterpret_cast<Item*>(wstage + kWarps);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(descs + kBufs);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(wstage + kWarps);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -177,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
     for (int i = 0; i < kBufs; ++i) mbar_init(&bars[i], 1);
     mbar_fence_init();
     for (int j = 0; j < kBufs && j < nmine; ++j)
-      issue_item(p, first + j * G, ring + j * kHeadDim * kHeadDim, &bars[j], &descs[j]);
+      issue_item(p, first + j * G, ring + j * kHeadDim * kHeadDim, &bars[j]);
   }
   __syncthreads();
 
@@ -207,12 +204,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
           s[i] = *reinterpret_cast<const float4*>(src + (tl.rg + 8 * i) * kHeadDim + tl.col);
       }
     }
-    // Every thread has read the slot and its descriptor: the slot can take
-    // the tile of item j + kBufs.
+    // Every thread has read the slot: it can take the tile of item j + kBufs.
     if (__syncthreads_or(!arrived)) break;
     if (threadIdx.x == 0 && j + kBufs < nmine)
       issue_item(p, first + (long long)(j + kBufs) * G, ring + buf * kHeadDim * kHeadDim,
-                 &bars[buf], &descs[buf]);
+                 &bars[buf]);
 
     if (!d.range_ok) {
       if (d.hv == 0 && threadIdx.x == 0) raise_status(p.dev_status, KDA_DEV_BAD_SEQLEN);
@@ -282,8 +278,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
 }  // namespace
 
 size_t decode_smem_bytes() {
-  return 128 + (size_t)kBufs * kTileBytes + kWarps * sizeof(TokenStage) + kBufs * sizeof(Item) +
-         kBufs * sizeof(uint64_t);
+  return 128 + (size_t)kBufs * kTileBytes + kWarps * sizeof(TokenStage) + kBufs * sizeof(uint64_t);
 }
 
 cudaError_t launch_kda_decode(const DecodeArgs& args, cudaStream_t stream) {
