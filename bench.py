@@ -476,14 +476,16 @@ def run_gpu(args, rank, world, local):
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = host_out[0].numel() * host_out[0].element_size()
     copy_stream = torch.cuda.Stream(dev)
+    out_stream = torch.cuda.Stream(dev)
     copied = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
     done = [torch.cuda.Event() for _ in range(2)]
 
     def copy_in(i):
         b = i % 2
         with torch.cuda.stream(copy_stream):
             if i >= 2:
-                copy_stream.wait_event(done[b])  # step i - 2 is done with this buffer
+                copy_stream.wait_event(computed[b])  # step i - 2's kernel is done with this buffer
             for k in keys:
                 dev_in[b][k].copy_(host[k], non_blocking=True)
             copied[b].record(copy_stream)
@@ -495,12 +497,17 @@ def run_gpu(args, rank, world, local):
             if i + 1 < n:
                 copy_in(i + 1)
             stream.wait_event(copied[b])
+            if i >= 2:
+                stream.wait_event(done[b])  # step i - 2's output has left this buffer
             kda_decode(dev_out[b], dev_in[b]["q"], dev_in[b]["k"], dev_in[b]["v"],
                        dev_in[b]["raw_gate"], dev_in[b]["beta_logits"], d["a_log"], d["dt_bias"],
                        dev_in[b]["cu_seqlens"], d["state_pool"], dev_in[b]["state_indices"],
                        gate_mode=inp["gate_mode"], lower_bound=inp["lower_bound"], stream=stream)
-            host_out[b].copy_(dev_out[b], non_blocking=True)
-            done[b].record(stream)
+            computed[b].record(stream)
+            with torch.cuda.stream(out_stream):  # read back while the next step computes
+                out_stream.wait_event(computed[b])
+                host_out[b].copy_(dev_out[b], non_blocking=True)
+                done[b].record(out_stream)
             if i >= 1:
                 done[(i - 1) % 2].synchronize()  # the host has step i - 1's output
         done[(n - 1) % 2].synchronize()
@@ -544,9 +551,10 @@ def run_gpu(args, rank, world, local):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "note": "every step: pinned host q/k/v/raw_gate/beta_logits/cu_seqlens/"
-                        "state_indices copied in (second stream, double-buffered, overlapping "
+                        "state_indices copied in (own stream, double-buffered, overlapping "
                         "the previous step's kernel) and the output copied back to pinned host "
-                        "memory, the host waiting for each step's output one step behind; "
+                        "memory (own stream, overlapping the next step's kernel), the host "
+                        "waiting for each step's output one step behind; "
                         "wall-clock time; state pool and model parameters resident on the device"},
         "gpu_launches": args.steps,
         "clocks": clocks,

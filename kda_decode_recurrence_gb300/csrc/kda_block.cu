@@ -34,8 +34,6 @@ namespace kda {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kLatCols = 64;   // latent GEMM: output columns per CTA
-constexpr int kLatRows = 32;   // latent GEMM: rows per CTA
 constexpr int kKS1 = 3;        // contraction splits of the W_in GEMM (99 tiles x 3 = 297 CTAs: one wave at 2 per SM)
 constexpr int kKS2 = 9;        // contraction splits of the W_o GEMM (32 tiles x 9 = 288 CTAs)
 
@@ -75,6 +73,22 @@ __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16* hi, __nv_bflo
   *lo = __float2bfloat16_rn(x - __bfloat162float(h));
 }
 
+// The same for four consecutive values, stored as one 8-byte word per half.
+__device__ __forceinline__ void split_bf16x4(float4 x, __nv_bfloat16* hi, __nv_bfloat16* lo) {
+  const __nv_bfloat162 h01 = __floats2bfloat162_rn(x.x, x.y);
+  const __nv_bfloat162 h23 = __floats2bfloat162_rn(x.z, x.w);
+  const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+  const __nv_bfloat162 l01 = __floats2bfloat162_rn(x.x - f01.x, x.y - f01.y);
+  const __nv_bfloat162 l23 = __floats2bfloat162_rn(x.z - f23.x, x.w - f23.y);
+  uint2 ph, pl;
+  ph.x = *reinterpret_cast<const uint32_t*>(&h01);
+  ph.y = *reinterpret_cast<const uint32_t*>(&h23);
+  pl.x = *reinterpret_cast<const uint32_t*>(&l01);
+  pl.y = *reinterpret_cast<const uint32_t*>(&l23);
+  *reinterpret_cast<uint2*>(hi) = ph;
+  *reinterpret_cast<uint2*>(lo) = pl;
+}
+
 __device__ __forceinline__ float block_sum(float x, float* red /* [kThreads/32] */) {
   x = warp_sum(x);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -99,12 +113,14 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_split_kernel(
   __shared__ float red[kNormThreads / 32];
   pdl_trigger();
   const float* x = hidden + (size_t)blockIdx.x * Hd;
-  float4 xv[kNormCache];
+  float4 xv[kNormCache], gv[kNormCache];
   float ss = 0.f;
 #pragma unroll
   for (int c = 0; c < kNormCache; ++c) {
     const int i = (threadIdx.x + c * kNormThreads) * 4;
-    xv[c] = i < Hd ? *reinterpret_cast<const float4*>(x + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const bool in = i < Hd;
+    xv[c] = in ? *reinterpret_cast<const float4*>(x + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    gv[c] = in ? *reinterpret_cast<const float4*>(gamma + i) : make_float4(0.f, 0.f, 0.f, 0.f);
     ss += xv[c].x * xv[c].x + xv[c].y * xv[c].y + xv[c].z * xv[c].z + xv[c].w * xv[c].w;
   }
   for (int i = (threadIdx.x + kNormCache * kNormThreads) * 4; i < Hd; i += kNormThreads * 4) {
@@ -121,87 +137,130 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_split_kernel(
   __nv_bfloat16* hi = X2 + (size_t)blockIdx.x * Hd;
   __nv_bfloat16* lo = X2 + ((size_t)R + blockIdx.x) * Hd;
   float* orow = out + (size_t)blockIdx.x * Hd;
-  auto emit = [&](int i, float4 v) {
-    const float4 g = *reinterpret_cast<const float4*>(gamma + i);
-    split_bf16(v.x * inv * g.x, hi + i + 0, lo + i + 0);
-    split_bf16(v.y * inv * g.y, hi + i + 1, lo + i + 1);
-    split_bf16(v.z * inv * g.z, hi + i + 2, lo + i + 2);
-    split_bf16(v.w * inv * g.w, hi + i + 3, lo + i + 3);
+  auto emit = [&](int i, float4 v, float4 g) {
+    split_bf16x4(make_float4(v.x * inv * g.x, v.y * inv * g.y, v.z * inv * g.z, v.w * inv * g.w),
+                 hi + i, lo + i);
     *reinterpret_cast<float4*>(orow + i) = make_float4(0.f, 0.f, 0.f, 0.f);
   };
 #pragma unroll
   for (int c = 0; c < kNormCache; ++c) {
     const int i = (threadIdx.x + c * kNormThreads) * 4;
-    if (i < Hd) emit(i, xv[c]);
+    if (i < Hd) emit(i, xv[c], gv[c]);
   }
   for (int i = (threadIdx.x + kNormCache * kNormThreads) * 4; i < Hd; i += kNormThreads * 4)
-    emit(i, *reinterpret_cast<const float4*>(x + i));
+    emit(i, *reinterpret_cast<const float4*>(x + i), *reinterpret_cast<const float4*>(gamma + i));
 }
 
 // 3. gate latents on the CUDA cores: gz[r][c] = f_a[r] . W_fb[:, c] for
 // c < CQ and g_a[r] . W_gb[:, c - CQ] after, with f_a and g_a summed from the
-// projection's split-K partials.  Grid ((CQ + CV) / 64, ceil(R / 32)), 256
-// threads.  The CTA first pulls its whole 128 x 64 weight tile and its
-// 32 x 128 activation panel into shared memory with 16-byte loads (one
-// round trip), then thread t computes columns 2 (t % 32) .. + 1 of rows
-// 4 (t / 32) .. + 3.
+// projection's split-K partials.  Grid ((CQ + CV) / 32, ceil(R / 32)), 256
+// threads; a CTA computes a 32-row x 32-column block.  Its weight tile
+// (128 x 32) is converted to fp32 in shared memory; the activation panel is
+// stored k-major.  Warp w takes contraction rows
+// [16w, 16w + 16) and lane (rb, cb) a 4-row x 8-column register block, so
+// each k costs three 16-byte shared loads for 32 FMAs; the eight warps'
+// partial blocks are then added through shared memory.
+constexpr int kLatTile = 32;                 // rows and columns per CTA
+constexpr int kLatKPerWarp = kHeadDim / 8;   // contraction rows per warp
+
 __global__ void __launch_bounds__(256) latent_kernel(
     const float* __restrict__ Ppart, int KS1, int R, int I, int off_fa, int off_ga,
     const kda_bf16* __restrict__ W_fb, int CQ, const kda_bf16* __restrict__ W_gb, int CV,
     float* __restrict__ gz) {
-  __shared__ __align__(16) float xs[kLatRows][kHeadDim];
-  __shared__ __align__(16) kda_bf16 ws[kHeadDim][kLatCols];
+  // Operands (xT 16 KiB + w 16 KiB), then reused for the partial sums.
+  __shared__ __align__(16) float buf[8 * kLatTile * kLatTile];
+  float (*xT)[kLatTile] = reinterpret_cast<float (*)[kLatTile]>(buf);                        // [k][r]
+  float (*wf)[kLatTile] = reinterpret_cast<float (*)[kLatTile]>(buf + kHeadDim * kLatTile);  // [k][c]
+  float (*part)[kLatTile * kLatTile] = reinterpret_cast<float (*)[kLatTile * kLatTile]>(buf);
+
   const int t = threadIdx.x;
-  const int c0 = blockIdx.x * kLatCols;
-  const bool is_fb = c0 < CQ;  // CQ is a multiple of 64
+  const int c0 = blockIdx.x * kLatTile;
+  const bool is_fb = c0 < CQ;  // CQ is a multiple of 32
   const kda_bf16* W = is_fb ? W_fb : W_gb;
   const int N = is_fb ? CQ : CV;
   const int cbase = is_fb ? c0 : c0 - CQ;
   const int off = is_fb ? off_fa : off_ga;
-  const int r0 = blockIdx.y * kLatRows;
+  const int r0 = blockIdx.y * kLatTile;
+
+  {  // weight tile: 128 rows x 32 bf16 = 4 x 16 bytes per row; 2 chunks per thread
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {  // 128 rows x 8 uint4
-    const int e = t + 256 * i, row = e >> 3, q = e & 7;
-    reinterpret_cast<uint4*>(&ws[row][0])[q] =
-        __ldg(reinterpret_cast<const uint4*>(W + (size_t)row * N + cbase) + q);
-  }
-  pdl_wait();  // the partial sums come from the projection GEMM
-  pdl_trigger();
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {  // 32 rows x 32 float4, summed over the splits
-    const int e = t + 256 * i, row = e >> 5, q = e & 31;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (r0 + row < R) {
-      for (int ks = 0; ks < KS1; ++ks) {
-        const float4 v = __ldg(reinterpret_cast<const float4*>(
-                                   Ppart + ((size_t)ks * R + r0 + row) * I + off) + q);
-        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-      }
+    for (int i = 0; i < 2; ++i) {
+      const int e = t + 256 * i, k = e >> 2, q = e & 3;
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(W + (size_t)k * N + cbase) + q);
+      float* dst = &wf[k][8 * q];
+      *reinterpret_cast<float4*>(dst) = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+      *reinterpret_cast<float4*>(dst + 4) =
+          make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
     }
-    reinterpret_cast<float4*>(&xs[row][0])[q] = acc;
+  }
+  pdl_wait();  // (a no-op: the kernel is launched in plain stream order)
+  pdl_trigger();
+  {  // activation panel, transposed: lane = row, so each k-row store is conflict-free
+    const int r = t & 31, kq0 = t >> 5;  // kq = 4-column group of k
+    const bool valid = r0 + r < R;
+    // All of the thread's partial-sum loads are issued before any is used:
+    // one L2 round trip instead of one per split and column group.
+    float4 v[4][kKS1];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int ks = 0; ks < kKS1; ++ks)
+        v[i][ks] = (valid && ks < KS1)
+                       ? __ldg(reinterpret_cast<const float4*>(
+                                   Ppart + ((size_t)ks * R + r0 + r) * I + off) + kq0 + 8 * i)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int kq = kq0 + 8 * i;
+      float4 acc = v[i][0];
+#pragma unroll
+      for (int ks = 1; ks < kKS1; ++ks) {
+        acc.x += v[i][ks].x; acc.y += v[i][ks].y; acc.z += v[i][ks].z; acc.w += v[i][ks].w;
+      }
+      xT[4 * kq + 0][r] = acc.x;
+      xT[4 * kq + 1][r] = acc.y;
+      xT[4 * kq + 2][r] = acc.z;
+      xT[4 * kq + 3][r] = acc.w;
+    }
   }
   __syncthreads();
-  const int cp = t & 31, rq = t >> 5;
-  float acc[4][2];
+  const int warp = t >> 5, lane = t & 31;
+  const int rb = lane >> 2, cb = lane & 3;  // rows 4rb..4rb+3, columns 8cb..8cb+7
+  float acc[4][8];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = 0.f;
-#pragma unroll 8
-  for (int k = 0; k < kHeadDim; ++k) {
-    const uint32_t w2 = *reinterpret_cast<const uint32_t*>(&ws[k][2 * cp]);
-    const float w0 = bf16_lo(w2), w1 = bf16_hi(w2);
+  for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float xv = xs[4 * rq + j][k];
-      acc[j][0] = fmaf(xv, w0, acc[j][0]);
-      acc[j][1] = fmaf(xv, w1, acc[j][1]);
-    }
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+#pragma unroll 4
+  for (int kk = 0; kk < kLatKPerWarp; ++kk) {
+    const int k = warp * kLatKPerWarp + kk;
+    const float4 x = *reinterpret_cast<const float4*>(&xT[k][4 * rb]);
+    const float4 wa = *reinterpret_cast<const float4*>(&wf[k][8 * cb]);
+    const float4 wb = *reinterpret_cast<const float4*>(&wf[k][8 * cb + 4]);
+    const float xv[4] = {x.x, x.y, x.z, x.w};
+    const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(xv[i], wv[j], acc[i][j]);
   }
+  __syncthreads();  // every warp is done with xT and wf: reuse them for the partials
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int r = r0 + 4 * rq + j;
-    if (r < R)
-      *reinterpret_cast<float2*>(gz + (size_t)r * (CQ + CV) + c0 + 2 * cp) =
-          make_float2(acc[j][0], acc[j][1]);
+  for (int i = 0; i < 4; ++i) {
+    float* dst = &part[warp][(4 * rb + i) * kLatTile + 8 * cb];
+    *reinterpret_cast<float4*>(dst) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+  }
+  __syncthreads();
+  {  // thread t: row t / 8, columns 4 (t % 8) .. + 3, summed over the warps in order
+    const int r = t >> 3, c4 = (t & 7) * 4;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const float4 v = *reinterpret_cast<const float4*>(&part[w][r * kLatTile + c4]);
+      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    }
+    if (r0 + r < R) *reinterpret_cast<float4*>(gz + (size_t)(r0 + r) * (CQ + CV) + c0 + c4) = s;
   }
 }
 
@@ -309,17 +368,28 @@ __global__ void __launch_bounds__(kPrepThreads, 1) block_prep_kernel(const PrepA
   for (int j = 0; j < p.n; ++j) {
     const int r = b * p.n + j;
     const float* prow = p.Ppart + (size_t)r * p.I;
-    float xq = 0.f, xk = 0.f, xv = 0.f, bl = 0.f;
-    for (int ks = 0; ks < p.KS1; ++ks) {
+    // Every load of the token is issued before any is used (one round trip).
+    float pq[kKS1], pk[kKS1], pv[kKS1], pb[kKS1];
+#pragma unroll
+    for (int ks = 0; ks < kKS1; ++ks) {
       const float* pr = prow + ks * pstride;
-      xq += pr[cq];
-      xk += pr[p.CQ + cq];
-      xv += pr[2 * p.CQ + cv];
-      bl += pr[off_beta + h];
+      const bool on = ks < p.KS1;
+      pq[ks] = on ? pr[cq] : 0.f;
+      pk[ks] = on ? pr[p.CQ + cq] : 0.f;
+      pv[ks] = on ? pr[2 * p.CQ + cv] : 0.f;
+      pb[ks] = on ? pr[off_beta + h] : 0.f;
     }
     const size_t gzrow = (size_t)r * (p.CQ + p.CV);
     const float graw = p.gz[gzrow + (size_t)h * kHeadDim + d];      // W_fb head-outer
     const float zz = p.gz[gzrow + p.CQ + (size_t)d * p.nh + h];     // W_gb channel-outer
+    float xq = pq[0], xk = pk[0], xv = pv[0], bl = pb[0];
+#pragma unroll
+    for (int ks = 1; ks < kKS1; ++ks) {
+      xq += pq[ks];
+      xk += pk[ks];
+      xv += pv[ks];
+      bl += pb[ks];
+    }
 
     if (j > 0) __syncthreads();  // the previous token's qs_, ks_ and red are consumed
     qs_[hq][dq] = conv_step(p, chq, xq);
@@ -443,8 +513,11 @@ cudaError_t launch_kda_block(const BlockArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int off_ga = 2 * L.CQ + L.CV;
   const int off_fa = off_ga + kHeadDim + a.nh;
-  e = launch(latent_kernel, dim3((L.CQ + L.CV) / kLatCols, (L.R + kLatRows - 1) / kLatRows),
-             dim3(256), 0, stream, true, (const float*)ppart, L.KS1, L.R, L.I, off_fa, off_ga,
+  // Not a programmatic dependent: launched early, its CTAs would be packed
+  // onto the first SMs the projection GEMM frees (several per SM, the other
+  // SMs idle); launched after the GEMM they spread over every SM.
+  e = launch(latent_kernel, dim3((L.CQ + L.CV) / kLatTile, (L.R + kLatTile - 1) / kLatTile),
+             dim3(256), 0, stream, false, (const float*)ppart, L.KS1, L.R, L.I, off_fa, off_ga,
              a.W_fb, L.CQ, a.W_gb, L.CV, gz);
   if (e != cudaSuccess) return e;
   TokenStage* stage = reinterpret_cast<TokenStage*>(ws + L.stage);

@@ -32,7 +32,8 @@
 namespace kda {
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kMaxWStages = 8;           // weight ring depth (chosen per launch)
+constexpr int kXStages = 2;              // activation ring depth (the activations sit in L2)
 constexpr int kBK = 64;                  // contraction rows per stage
 constexpr int kTileN = 128;              // weight columns per CTA (MMA M)
 constexpr int kABytes = kBK * kTileN * 2;  // 16 KiB: two 64x64 swizzled boxes
@@ -101,10 +102,15 @@ struct GemmShape {
   int N;           // output columns (multiple of 8)
   int KS;          // contraction splits
   int accumulate;  // add each split into Y[r][n] instead of writing Ypart[ks]
+  int wstages;     // weight ring depth, 2..kMaxWStages
 };
 
-// Dynamic shared memory: kStages x (A 16 KiB + B 2*RB*128 B), 1024-aligned,
-// followed by the mbarriers and the TMEM base address word.
+// Dynamic shared memory, 1024-aligned: the weight ring (wstages x 16 KiB A
+// tiles), the activation ring (kXStages x 2*RB*128 B B tiles), then the
+// mbarriers and the TMEM base address word.  The two rings have their own
+// producers and barriers, so the weight stream runs as far ahead as the
+// weight ring allows while the small activation tiles (L2 hits) follow two
+// stages behind.
 __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
     const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
     float* __restrict__ Ypart, const GemmShape sh, int32_t* __restrict__ err) {
@@ -121,20 +127,28 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
   const int NM = 2 * RB;                   // MMA N
   const uint32_t tmem_cols = NM <= 64 ? 64 : (NM <= 128 ? 128 : 256);
   const int b_bytes = NM * 128;            // hi and lo boxes, 128 B per token row
-  const int stage_bytes = kABytes + b_bytes;
+  const int nW = sh.wstages;
   const int nkb = sh.Kdim / kBK;
   const int kb0 = (int)((long long)ks * nkb / sh.KS);
   const int kb1 = (int)((long long)(ks + 1) * nkb / sh.KS);
 
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * stage_bytes);
-  uint64_t* empty = full + kStages;
-  uint64_t* done = empty + kStages;
+  unsigned char* wring = smem;
+  unsigned char* xring = smem + nW * kABytes;
+  uint64_t* wfull = reinterpret_cast<uint64_t*>(xring + kXStages * b_bytes);
+  uint64_t* wempty = wfull + kMaxWStages;
+  uint64_t* xfull = wempty + kMaxWStages;
+  uint64_t* xempty = xfull + kXStages;
+  uint64_t* done = xempty + kXStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < nW; ++s) {
+      mbar_init(&wfull[s], 1);
+      mbar_init(&wempty[s], 1);
+    }
+    for (int s = 0; s < kXStages; ++s) {
+      mbar_init(&xfull[s], 1);
+      mbar_init(&xempty[s], 1);
     }
     mbar_init(done, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -151,15 +165,15 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // The weights do not depend on the preceding kernel: the first stages'
-  // weight tiles are requested before waiting for it.
-  const int pre = min(kStages, kb1 - kb0);
+  // The weights do not depend on the preceding kernel: the whole weight ring
+  // is requested before waiting for it.
+  const int pre = min(nW, kb1 - kb0);
   if (warp == 0 && lane == 0) {
     for (int i = 0; i < pre; ++i) {
-      unsigned char* a_s = smem + i * stage_bytes;
-      mbar_expect_tx(&full[i], stage_bytes);
-      tma_load_2d(a_s, &tmW, &full[i], n0, (kb0 + i) * kBK);
-      tma_load_2d(a_s + kABytes / 2, &tmW, &full[i], n0 + 64, (kb0 + i) * kBK);
+      unsigned char* a_s = wring + i * kABytes;
+      mbar_expect_tx(&wfull[i], kABytes);
+      tma_load_2d(a_s, &tmW, &wfull[i], n0, (kb0 + i) * kBK);
+      tma_load_2d(a_s + kABytes / 2, &tmW, &wfull[i], n0 + 64, (kb0 + i) * kBK);
     }
   }
   pdl_wait();
@@ -167,32 +181,40 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
 
   bool ok = true;
   if (warp == 0 && lane == 0) {
-    // TMA producer
+    // weight producer
+    for (int kb = kb0 + pre; kb < kb1 && ok; ++kb) {
+      const int i = kb - kb0, s = i % nW, round = i / nW;
+      if (!mbar_wait(&wempty[s], (round - 1) & 1)) { ok = false; break; }
+      unsigned char* a_s = wring + s * kABytes;
+      mbar_expect_tx(&wfull[s], kABytes);
+      tma_load_2d(a_s, &tmW, &wfull[s], n0, kb * kBK);
+      tma_load_2d(a_s + kABytes / 2, &tmW, &wfull[s], n0 + 64, kb * kBK);
+    }
+  } else if (warp == 2 && lane == 0) {
+    // activation producer
     for (int kb = kb0; kb < kb1 && ok; ++kb) {
-      const int i = kb - kb0, s = i % kStages, round = i / kStages;
-      unsigned char* a_s = smem + s * stage_bytes;
-      unsigned char* b_s = a_s + kABytes;
+      const int i = kb - kb0, s = i % kXStages, round = i / kXStages;
+      if (i >= kXStages && !mbar_wait(&xempty[s], (round - 1) & 1)) { ok = false; break; }
+      unsigned char* b_s = xring + s * b_bytes;
       const int k0 = kb * kBK;
-      if (i >= pre) {
-        if (!mbar_wait(&empty[s], (round - 1) & 1)) { ok = false; break; }
-        mbar_expect_tx(&full[s], stage_bytes);
-        tma_load_2d(a_s, &tmW, &full[s], n0, k0);
-        tma_load_2d(a_s + kABytes / 2, &tmW, &full[s], n0 + 64, k0);
-      }
+      mbar_expect_tx(&xfull[s], b_bytes);
       for (int j = 0; j < RB / kBoxRows; ++j) {
-        tma_load_2d(b_s + j * kBoxRows * 128, &tmX, &full[s], k0, r0 + j * kBoxRows);
-        tma_load_2d(b_s + (RB + j * kBoxRows) * 128, &tmX, &full[s], k0, sh.R + r0 + j * kBoxRows);
+        tma_load_2d(b_s + j * kBoxRows * 128, &tmX, &xfull[s], k0, r0 + j * kBoxRows);
+        tma_load_2d(b_s + (RB + j * kBoxRows) * 128, &tmX, &xfull[s], k0, sh.R + r0 + j * kBoxRows);
       }
     }
   } else if (warp == 1 && lane == 0) {
     // MMA issuer
     const uint32_t idesc = instr_desc_bf16(NM, kTileN);
     for (int kb = kb0; kb < kb1 && ok; ++kb) {
-      const int i = kb - kb0, s = i % kStages, round = i / kStages;
-      if (!mbar_wait(&full[s], round & 1)) { ok = false; break; }
+      const int i = kb - kb0, sw = i % nW, sx = i % kXStages;
+      if (!mbar_wait(&wfull[sw], (i / nW) & 1) || !mbar_wait(&xfull[sx], (i / kXStages) & 1)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
-      const uint32_t a_addr = smem_u32(smem + s * stage_bytes);
-      const uint32_t b_addr = a_addr + kABytes;
+      const uint32_t a_addr = smem_u32(wring + sw * kABytes);
+      const uint32_t b_addr = smem_u32(xring + sx * b_bytes);
 #pragma unroll
       for (int j = 0; j < kBK / 16; ++j) {
         // A: MN-major, atoms of 64 columns x 8 rows; next column atom 8 KiB
@@ -202,7 +224,8 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
         const uint64_t bdesc = smem_desc_sw128(b_addr + j * 32, 16, 1024);
         mma_bf16(tmem, adesc, bdesc, idesc, (kb > kb0 || j > 0) ? 1u : 0u);
       }
-      mma_commit(&empty[s]);
+      mma_commit(&wempty[sw]);
+      mma_commit(&xempty[sx]);
     }
     mma_commit(done);
   }
@@ -256,10 +279,26 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer
 
 }  // namespace
 
-size_t tc_gemm_smem_bytes(int R) {
+// Ring depths for R token rows: the deepest weight ring that still lets two
+// CTAs share an SM (113 KiB each), else the deepest that fits one CTA.
+static void gemm_rings(int R, int* wstages, size_t* smem) {
   const int rows = R < 128 ? R : 128;
   const int RB = (rows + 31) & ~31;
-  return 1024 + (size_t)kStages * (kABytes + 2 * RB * 128) + (2 * kStages + 1) * 8 + 16;
+  const size_t fixed = 1024 + (size_t)kXStages * 2 * RB * 128 +
+                       (2 * kMaxWStages + 2 * kXStages + 1) * 8 + 16;
+  const size_t two_per_sm = 113 * 1024, one_per_sm = 227 * 1024;
+  int w = (int)((two_per_sm - fixed) / kABytes);
+  if (fixed > two_per_sm || w < 4) w = (int)((one_per_sm - fixed) / kABytes);
+  if (w > kMaxWStages) w = kMaxWStages;
+  *wstages = w;
+  *smem = fixed + (size_t)w * kABytes;
+}
+
+size_t tc_gemm_smem_bytes(int R) {
+  int w;
+  size_t smem;
+  gemm_rings(R, &w, &smem);
+  return smem;
 }
 
 cudaError_t launch_tc_gemm(const kda_bf16* X2, int R, int Kdim, const kda_bf16* W, int N, int KS,
@@ -270,11 +309,13 @@ cudaError_t launch_tc_gemm(const kda_bf16* X2, int R, int Kdim, const kda_bf16* 
   CUtensorMap tmW, tmX;
   if (!make_map(&tmW, W, (uint64_t)N, (uint64_t)Kdim, kBK)) return cudaErrorInvalidValue;
   if (!make_map(&tmX, X2, (uint64_t)Kdim, (uint64_t)2 * R, kBoxRows)) return cudaErrorInvalidValue;
-  const size_t smem = tc_gemm_smem_bytes(R);
+  int wstages;
+  size_t smem;
+  gemm_rings(R, &wstages, &smem);
   cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  GemmShape sh{R, Kdim, N, KS, accumulate ? 1 : 0};
+  GemmShape sh{R, Kdim, N, KS, accumulate ? 1 : 0, wstages};
   dim3 grid((N + kTileN - 1) / kTileN, KS, (R + 127) / 128);
   return launch(tc_gemm_kernel, grid, dim3(128), smem, stream, pdl, tmW, tmX, Ypart, sh, err);
 }
