@@ -10,10 +10,11 @@
 // b, R = B * n):
 //   1. rmsnorm      x = hidden * rsqrt(mean(hidden^2) + eps) * gamma_in, written
 //                   as bf16 hi/lo halves X2 [2R, Hd] for the tensor cores; out
-//                   zeroed
+//                   and the projection tail zeroed
 //   2. proj GEMM    tcgen05, P_part[ks] = x[:, split ks] . W_in[split ks, :]   [KS1, R, I]
 //                   (split-K so every SM streams a slice of the 103 MB W_in;
-//                   consumers add the KS1 partial sums)
+//                   consumers add the KS1 partial sums of q, k, v; the g_a,
+//                   beta, f_a columns are summed in place into `tail`)
 //   3. latent       graw = f_a . W_fb, z = g_a . W_gb (CUDA cores)            [R, CQ + CV]
 //   4. prep         one CTA per (b, 8 heads), channels read coalesced: short
 //                   conv + SiLU + conv_state update of the q, k, v channels,
@@ -39,7 +40,8 @@ constexpr int kKS2 = 9;        // contraction splits of the W_o GEMM (32 tiles x
 
 struct Layout {
   int R, I, CQ, CV, KS1, KS2;
-  size_t x2, ppart, gz, stage, zgate, on2, err, total;
+  int TC, TN;  // projection columns >= TC (g_a, beta, f_a): TN of them, summed in place
+  size_t x2, ppart, tail, gz, stage, zgate, on2, err, total;
 };
 
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -52,11 +54,14 @@ bool make_layout(int B, int n, int Hd, int nh, int K, int V, int Kc, Layout* L) 
   L->CQ = K * nh;
   L->CV = V * nh;
   L->I = 2 * L->CQ + L->CV + 2 * K + nh;
+  L->TC = 2 * L->CQ + L->CV;  // a multiple of 128
+  L->TN = L->I - L->TC;
   L->KS1 = Hd / 64 < kKS1 ? Hd / 64 : kKS1;        // splits <= 64-row contraction blocks
   L->KS2 = L->CV / 64 < kKS2 ? L->CV / 64 : kKS2;
   size_t off = 0;
   L->x2 = off;    off = align_up(off + 2 * sizeof(kda_bf16) * (size_t)L->R * Hd);
   L->ppart = off; off = align_up(off + sizeof(float) * (size_t)L->KS1 * L->R * L->I);
+  L->tail = off;  off = align_up(off + sizeof(float) * (size_t)L->R * L->TN);
   L->gz = off;    off = align_up(off + sizeof(float) * (size_t)L->R * (L->CQ + L->CV));
   L->stage = off; off = align_up(off + sizeof(TokenStage) * (size_t)L->R * nh);
   L->zgate = off; off = align_up(off + sizeof(float) * (size_t)L->R * L->CV);
@@ -109,7 +114,8 @@ constexpr int kNormCache = 4;  // float4 per thread held in registers (Hd <= 163
 // `out`, which the output projection accumulates into.
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_split_kernel(
     const float* __restrict__ hidden, const float* __restrict__ gamma,
-    __nv_bfloat16* __restrict__ X2, float* __restrict__ out, int R, int Hd, float eps) {
+    __nv_bfloat16* __restrict__ X2, float* __restrict__ out, float* __restrict__ tail, int TN,
+    int R, int Hd, float eps) {
   __shared__ float red[kNormThreads / 32];
   pdl_trigger();
   const float* x = hidden + (size_t)blockIdx.x * Hd;
@@ -137,6 +143,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_split_kernel(
   __nv_bfloat16* hi = X2 + (size_t)blockIdx.x * Hd;
   __nv_bfloat16* lo = X2 + ((size_t)R + blockIdx.x) * Hd;
   float* orow = out + (size_t)blockIdx.x * Hd;
+  for (int i = threadIdx.x; i < TN; i += kNormThreads) tail[(size_t)blockIdx.x * TN + i] = 0.f;
   auto emit = [&](int i, float4 v, float4 g) {
     split_bf16x4(make_float4(v.x * inv * g.x, v.y * inv * g.y, v.z * inv * g.z, v.w * inv * g.w),
                  hi + i, lo + i);
@@ -152,8 +159,9 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_split_kernel(
 }
 
 // 3. gate latents on the CUDA cores: gz[r][c] = f_a[r] . W_fb[:, c] for
-// c < CQ and g_a[r] . W_gb[:, c - CQ] after, with f_a and g_a summed from the
-// projection's split-K partials.  Grid ((CQ + CV) / 32, ceil(R / 32)), 256
+// c < CQ and g_a[r] . W_gb[:, c - CQ] after, with f_a and g_a read from the
+// projection (Ppart holds KS1 partial sums to add; the block passes the
+// in-place tail with KS1 = 1).  Grid ((CQ + CV) / 32, ceil(R / 32)), 256
 // threads; a CTA computes a 32-row x 32-column block.  Its weight tile
 // (128 x 32) is converted to fp32 in shared memory; the activation panel is
 // stored k-major.  Warp w takes contraction rows
@@ -266,6 +274,7 @@ __global__ void __launch_bounds__(256) latent_kernel(
 
 struct PrepArgs {
   const float* Ppart;
+  const float* tail;  // [R, TN]: g_a, beta, f_a summed over the splits
   const float* gz;
   const kda_bf16* conv_w;
   float* conv_state;
@@ -275,7 +284,7 @@ struct PrepArgs {
   TokenStage* stage;  // [R, nh]
   float* zgate;       // [R, nh, V]: gamma_o[d] * sigmoid(z)
   float scale, lower_bound, l2_eps;
-  int R, n, I, KS1, nh, Kc, CQ, CV;
+  int R, n, I, KS1, nh, Kc, CQ, CV, TN;
 };
 
 // One channel of the depthwise causal conv: the window is conv_state[b, s, c,
@@ -349,7 +358,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) block_prep_kernel(const PrepA
   const int h = h0 + hl;
   const int cv = h * kHeadDim + d;
   const size_t pstride = (size_t)p.R * p.I;
-  const int off_beta = 2 * p.CQ + p.CV + kHeadDim;
+
   const int w = t >> 5;
   const int w0 = hl * (kHeadDim / 32);  // the 4 warps of head hl
 
@@ -369,7 +378,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) block_prep_kernel(const PrepA
     const int r = b * p.n + j;
     const float* prow = p.Ppart + (size_t)r * p.I;
     // Every load of the token is issued before any is used (one round trip).
-    float pq[kKS1], pk[kKS1], pv[kKS1], pb[kKS1];
+    float pq[kKS1], pk[kKS1], pv[kKS1];
 #pragma unroll
     for (int ks = 0; ks < kKS1; ++ks) {
       const float* pr = prow + ks * pstride;
@@ -377,18 +386,17 @@ __global__ void __launch_bounds__(kPrepThreads, 1) block_prep_kernel(const PrepA
       pq[ks] = on ? pr[cq] : 0.f;
       pk[ks] = on ? pr[p.CQ + cq] : 0.f;
       pv[ks] = on ? pr[2 * p.CQ + cv] : 0.f;
-      pb[ks] = on ? pr[off_beta + h] : 0.f;
     }
     const size_t gzrow = (size_t)r * (p.CQ + p.CV);
     const float graw = p.gz[gzrow + (size_t)h * kHeadDim + d];      // W_fb head-outer
     const float zz = p.gz[gzrow + p.CQ + (size_t)d * p.nh + h];     // W_gb channel-outer
-    float xq = pq[0], xk = pk[0], xv = pv[0], bl = pb[0];
+    const float bl = p.tail[(size_t)r * p.TN + kHeadDim + h];
+    float xq = pq[0], xk = pk[0], xv = pv[0];
 #pragma unroll
     for (int ks = 1; ks < kKS1; ++ks) {
       xq += pq[ks];
       xk += pk[ks];
       xv += pv[ks];
-      bl += pb[ks];
     }
 
     if (j > 0) __syncthreads();  // the previous token's qs_, ks_ and red are consumed
@@ -498,6 +506,7 @@ cudaError_t launch_kda_block(const BlockArgs& a, cudaStream_t stream) {
   char* ws = static_cast<char*>(a.workspace);
   __nv_bfloat16* x2 = reinterpret_cast<__nv_bfloat16*>(ws + L.x2);
   float* ppart = reinterpret_cast<float*>(ws + L.ppart);
+  float* tail = reinterpret_cast<float*>(ws + L.tail);
   float* gz = reinterpret_cast<float*>(ws + L.gz);
   __nv_bfloat16* on2 = reinterpret_cast<__nv_bfloat16*>(ws + L.on2);
   int32_t* err = a.dev_status ? a.dev_status : reinterpret_cast<int32_t*>(ws + L.err);
@@ -506,24 +515,30 @@ cudaError_t launch_kda_block(const BlockArgs& a, cudaStream_t stream) {
   // The first kernel waits for everything before it in the stream; each later
   // kernel is a programmatic dependent of the one before it.
   e = launch(rmsnorm_split_kernel, dim3(L.R), dim3(kNormThreads), 0, stream, false, a.hidden,
-             a.gamma_in, x2, a.out, L.R, a.Hd, a.rms_norm_eps);
+             a.gamma_in, x2, a.out, tail, L.TN, L.R, a.Hd, a.rms_norm_eps);
   if (e != cudaSuccess) return e;
+  // g_a, beta and f_a (the last TN columns) are summed over the splits in
+  // place (into `tail`, zeroed by the RMSNorm kernel): every latent CTA reads
+  // the f_a / g_a panel, so it is kept at one copy.
   e = launch_tc_gemm(reinterpret_cast<const kda_bf16*>(x2), L.R, a.Hd, a.W_in, L.I, L.KS1, ppart,
-                     false, err, stream, true);
+                     false, err, stream, true, tail, L.TC);
   if (e != cudaSuccess) return e;
-  const int off_ga = 2 * L.CQ + L.CV;
-  const int off_fa = off_ga + kHeadDim + a.nh;
+  // Within the tail: g_a at 0, beta at K, f_a at K + nh.
+  const int off_ga = 0;
+  const int off_fa = kHeadDim + a.nh;
   // Not a programmatic dependent: launched early, its CTAs would be packed
   // onto the first SMs the projection GEMM frees (several per SM, the other
   // SMs idle); launched after the GEMM they spread over every SM.
   e = launch(latent_kernel, dim3((L.CQ + L.CV) / kLatTile, (L.R + kLatTile - 1) / kLatTile),
-             dim3(256), 0, stream, false, (const float*)ppart, L.KS1, L.R, L.I, off_fa, off_ga,
+             dim3(256), 0, stream, false, (const float*)tail, 1, L.R, L.TN, off_fa, off_ga,
              a.W_fb, L.CQ, a.W_gb, L.CV, gz);
   if (e != cudaSuccess) return e;
   TokenStage* stage = reinterpret_cast<TokenStage*>(ws + L.stage);
   float* zgate = reinterpret_cast<float*>(ws + L.zgate);
   PrepArgs pa;
   pa.Ppart = ppart;
+  pa.tail = tail;
+  pa.TN = L.TN;
   pa.gz = gz;
   pa.conv_w = a.conv_w;
   pa.conv_state = a.conv_state;

@@ -33,7 +33,7 @@ namespace kda {
 namespace {
 
 constexpr int kMaxWStages = 8;           // weight ring depth (chosen per launch)
-constexpr int kXStages = 2;              // activation ring depth (the activations sit in L2)
+constexpr int kMaxXStages = 4;           // activation ring depth (chosen per launch)
 constexpr int kBK = 64;                  // contraction rows per stage
 constexpr int kTileN = 128;              // weight columns per CTA (MMA M)
 constexpr int kABytes = kBK * kTileN * 2;  // 16 KiB: two 64x64 swizzled boxes
@@ -103,14 +103,17 @@ struct GemmShape {
   int KS;          // contraction splits
   int accumulate;  // add each split into Y[r][n] instead of writing Ypart[ks]
   int wstages;     // weight ring depth, 2..kMaxWStages
+  int xstages;     // activation ring depth, 2..kMaxXStages
+  float* tail;     // optional: columns >= tail_col are added (fp32 atomics)
+  int tail_col;    // into tail[r][n - tail_col] (row stride tail_n) instead
+  int tail_n;      // of being written per split
 };
 
 // Dynamic shared memory, 1024-aligned: the weight ring (wstages x 16 KiB A
-// tiles), the activation ring (kXStages x 2*RB*128 B B tiles), then the
+// tiles), the activation ring (xstages x 2*RB*128 B B tiles), then the
 // mbarriers and the TMEM base address word.  The two rings have their own
-// producers and barriers, so the weight stream runs as far ahead as the
-// weight ring allows while the small activation tiles (L2 hits) follow two
-// stages behind.
+// producers and barriers, so the weight stream (HBM) runs as far ahead as
+// its ring allows while the activation tiles (L2 hits) follow their own.
 __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
     const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
     float* __restrict__ Ypart, const GemmShape sh, int32_t* __restrict__ err) {
@@ -127,18 +130,18 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
   const int NM = 2 * RB;                   // MMA N
   const uint32_t tmem_cols = NM <= 64 ? 64 : (NM <= 128 ? 128 : 256);
   const int b_bytes = NM * 128;            // hi and lo boxes, 128 B per token row
-  const int nW = sh.wstages;
+  const int nW = sh.wstages, nX = sh.xstages;
   const int nkb = sh.Kdim / kBK;
   const int kb0 = (int)((long long)ks * nkb / sh.KS);
   const int kb1 = (int)((long long)(ks + 1) * nkb / sh.KS);
 
   unsigned char* wring = smem;
   unsigned char* xring = smem + nW * kABytes;
-  uint64_t* wfull = reinterpret_cast<uint64_t*>(xring + kXStages * b_bytes);
+  uint64_t* wfull = reinterpret_cast<uint64_t*>(xring + nX * b_bytes);
   uint64_t* wempty = wfull + kMaxWStages;
   uint64_t* xfull = wempty + kMaxWStages;
-  uint64_t* xempty = xfull + kXStages;
-  uint64_t* done = xempty + kXStages;
+  uint64_t* xempty = xfull + kMaxXStages;
+  uint64_t* done = xempty + kMaxXStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
 
   if (threadIdx.x == 0) {
@@ -146,7 +149,7 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
       mbar_init(&wfull[s], 1);
       mbar_init(&wempty[s], 1);
     }
-    for (int s = 0; s < kXStages; ++s) {
+    for (int s = 0; s < nX; ++s) {
       mbar_init(&xfull[s], 1);
       mbar_init(&xempty[s], 1);
     }
@@ -193,8 +196,8 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
   } else if (warp == 2 && lane == 0) {
     // activation producer
     for (int kb = kb0; kb < kb1 && ok; ++kb) {
-      const int i = kb - kb0, s = i % kXStages, round = i / kXStages;
-      if (i >= kXStages && !mbar_wait(&xempty[s], (round - 1) & 1)) { ok = false; break; }
+      const int i = kb - kb0, s = i % nX, round = i / nX;
+      if (i >= nX && !mbar_wait(&xempty[s], (round - 1) & 1)) { ok = false; break; }
       unsigned char* b_s = xring + s * b_bytes;
       const int k0 = kb * kBK;
       mbar_expect_tx(&xfull[s], b_bytes);
@@ -207,8 +210,8 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
     // MMA issuer
     const uint32_t idesc = instr_desc_bf16(NM, kTileN);
     for (int kb = kb0; kb < kb1 && ok; ++kb) {
-      const int i = kb - kb0, sw = i % nW, sx = i % kXStages;
-      if (!mbar_wait(&wfull[sw], (i / nW) & 1) || !mbar_wait(&xfull[sx], (i / kXStages) & 1)) {
+      const int i = kb - kb0, sw = i % nW, sx = i % nX;
+      if (!mbar_wait(&wfull[sw], (i / nW) & 1) || !mbar_wait(&xfull[sx], (i / nX) & 1)) {
         ok = false;
         break;
       }
@@ -239,6 +242,7 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
   }
   tc_fence_after();
   const int m = n0 + warp * 32 + lane;
+  const bool to_tail = sh.tail != nullptr && n0 >= sh.tail_col;  // whole tiles
   if (have) {
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     for (int c = 0; c < RB / 32; ++c) {
@@ -251,7 +255,9 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
         for (int j = 0; j < 32; ++j) {
           const int r = r0 + c * 32 + j;
           if (r < sh.R) {
-            if (sh.accumulate)
+            if (to_tail)
+              atomicAdd(sh.tail + (size_t)r * sh.tail_n + (m - sh.tail_col), hi[j] + lo[j]);
+            else if (sh.accumulate)
               atomicAdd(Ypart + (size_t)r * sh.N + m, hi[j] + lo[j]);
             else
               Ypart[((size_t)ks * sh.R + r) * sh.N + m] = hi[j] + lo[j];
@@ -279,43 +285,50 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer
 
 }  // namespace
 
-// Ring depths for R token rows: the deepest weight ring that still lets two
-// CTAs share an SM (113 KiB each), else the deepest that fits one CTA.
-static void gemm_rings(int R, int* wstages, size_t* smem) {
+// Ring depths for R token rows.  Every CTA streams its weight slice once
+// from HBM but re-reads the activations of its contraction range from L2,
+// 2*RB*128 bytes per 16 KiB weight stage, so for 32 rows (8 KiB per stage)
+// two activation stages suffice and two CTAs share an SM (113 KiB each) with
+// the deepest weight ring that fits; larger row blocks take one CTA per SM
+// (227 KiB) and four activation stages.
+static void gemm_rings(int R, int* wstages, int* xstages, size_t* smem) {
   const int rows = R < 128 ? R : 128;
   const int RB = (rows + 31) & ~31;
-  const size_t fixed = 1024 + (size_t)kXStages * 2 * RB * 128 +
-                       (2 * kMaxWStages + 2 * kXStages + 1) * 8 + 16;
-  const size_t two_per_sm = 113 * 1024, one_per_sm = 227 * 1024;
-  int w = (int)((two_per_sm - fixed) / kABytes);
-  if (fixed > two_per_sm || w < 4) w = (int)((one_per_sm - fixed) / kABytes);
+  const size_t b_bytes = (size_t)2 * RB * 128;
+  const size_t extra = 1024 + (2 * kMaxWStages + 2 * kMaxXStages + 1) * 8 + 16;
+  const size_t budget = RB <= 32 ? 113 * 1024 : 227 * 1024;
+  const int x = RB <= 32 ? 2 : kMaxXStages;
+  int w = (int)((budget - extra - x * b_bytes) / kABytes);
   if (w > kMaxWStages) w = kMaxWStages;
   *wstages = w;
-  *smem = fixed + (size_t)w * kABytes;
+  *xstages = x;
+  *smem = extra + x * b_bytes + (size_t)w * kABytes;
 }
 
 size_t tc_gemm_smem_bytes(int R) {
-  int w;
+  int w, x;
   size_t smem;
-  gemm_rings(R, &w, &smem);
+  gemm_rings(R, &w, &x, &smem);
   return smem;
 }
 
 cudaError_t launch_tc_gemm(const kda_bf16* X2, int R, int Kdim, const kda_bf16* W, int N, int KS,
                            float* Ypart, bool accumulate, int32_t* err, cudaStream_t stream,
-                           bool pdl) {
-  if (R < 1 || Kdim % kBK != 0 || N % 8 != 0 || KS < 1 || KS > Kdim / kBK)
+                           bool pdl, float* tail, int tail_col) {
+  if (R < 1 || Kdim % kBK != 0 || N % 8 != 0 || KS < 1 || KS > Kdim / kBK ||
+      (tail && (tail_col % kTileN != 0 || tail_col < 0 || tail_col >= N)))
     return cudaErrorInvalidValue;
   CUtensorMap tmW, tmX;
   if (!make_map(&tmW, W, (uint64_t)N, (uint64_t)Kdim, kBK)) return cudaErrorInvalidValue;
   if (!make_map(&tmX, X2, (uint64_t)Kdim, (uint64_t)2 * R, kBoxRows)) return cudaErrorInvalidValue;
-  int wstages;
+  int wstages, xstages;
   size_t smem;
-  gemm_rings(R, &wstages, &smem);
+  gemm_rings(R, &wstages, &xstages, &smem);
   cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  GemmShape sh{R, Kdim, N, KS, accumulate ? 1 : 0, wstages};
+  GemmShape sh{R, Kdim, N, KS, accumulate ? 1 : 0, wstages, xstages, tail, tail_col,
+               N - tail_col};
   dim3 grid((N + kTileN - 1) / kTileN, KS, (R + 127) / 128);
   return launch(tc_gemm_kernel, grid, dim3(128), smem, stream, pdl, tmW, tmX, Ypart, sh, err);
 }

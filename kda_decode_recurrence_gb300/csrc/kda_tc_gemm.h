@@ -18,9 +18,13 @@ namespace kda {
 // bit 1 into *err (a device int32) and leaves Ypart incomplete.  With `pdl`
 // the kernel is a programmatic dependent of the previous kernel in the stream
 // (it requests its first weight tiles before waiting for that kernel).
+// With `tail` (fp32 [R, N - tail_col], holding the starting value, e.g.
+// zeros; tail_col a multiple of 128), the columns n >= tail_col are summed
+// over the splits into tail[r][n - tail_col] with fp32 atomics instead of
+// being written to Ypart.
 cudaError_t launch_tc_gemm(const kda_bf16* X2, int R, int Kdim, const kda_bf16* W, int N, int KS,
                            float* Ypart, bool accumulate, int32_t* err, cudaStream_t stream,
-                           bool pdl);
+                           bool pdl, float* tail = nullptr, int tail_col = 0);
 
 size_t tc_gemm_smem_bytes(int R);
 
