@@ -448,10 +448,9 @@ struct RecArgs {
 // in registers across the request's n tokens; per token the staged vectors
 // are read, one delta-rule step is taken and the gated output RMSNorm is
 // written as bf16 hi/lo for the output projection.
-// kMulti: the n > 1 form (more registers for the token loop, 1 CTA per SM);
-// the n = 1 form keeps 2 CTAs per SM.
+// kMulti: the n > 1 form (the token loop); both forms fit two CTAs per SM.
 template <bool kMulti>
-__global__ void __launch_bounds__(kThreads, kMulti ? 1 : 2) block_recurrence_kernel(const RecArgs p) {
+__global__ void __launch_bounds__(kThreads, 2) block_recurrence_kernel(const RecArgs p) {
   __shared__ TokenStage ts;
   __shared__ __align__(16) float zg[kHeadDim];
   __shared__ __align__(16) float o_s[kHeadDim];

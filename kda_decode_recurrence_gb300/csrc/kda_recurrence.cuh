@@ -64,6 +64,10 @@ __device__ __forceinline__ float4 tile_token_step(float4 (&s)[16], const TokenSt
   float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
+    // A compiler-only fence halfway: it keeps the compiler from hoisting all
+    // sixteen 16-byte row loads ahead of the arithmetic, which with the 64
+    // tile registers live exceeds the 128-register budget and spills.
+    if (i == 8) asm volatile("" ::: "memory");
     const RowCoef rc = ts.row[tl.rg + 8 * i];
     s[i].x *= rc.decay; s[i].y *= rc.decay; s[i].z *= rc.decay; s[i].w *= rc.decay;
     a.x = fmaf(rc.kh, s[i].x, a.x); a.y = fmaf(rc.kh, s[i].y, a.y);
@@ -82,6 +86,7 @@ __device__ __forceinline__ float4 tile_token_step(float4 (&s)[16], const TokenSt
   const float4 u = make_float4(vv.x - a.x, vv.y - a.y, vv.z - a.z, vv.w - a.w);
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
+    if (i == 8) asm volatile("" ::: "memory");  // as above
     const float bkh = ts.row[tl.rg + 8 * i].bkh;
     s[i].x = fmaf(bkh, u.x, s[i].x); s[i].y = fmaf(bkh, u.y, s[i].y);
     s[i].z = fmaf(bkh, u.z, s[i].z); s[i].w = fmaf(bkh, u.w, s[i].w);
