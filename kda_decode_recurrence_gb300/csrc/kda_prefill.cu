@@ -23,6 +23,7 @@
 // One 256-thread CTA per (request, value head); the [128, 128] state tile is
 // held in registers in the layout of kda_decode (warp w: value columns
 // 16w .. 16w + 15; lane = (row group rg, column quad cg); rows rg + 8i).
+#include "kda_async.cuh"
 #include "kda_recurrence.cuh"
 
 namespace kda {
@@ -69,6 +70,15 @@ __device__ __forceinline__ ChunkIn fetch(const DecodeArgs& p, int t, int h, int 
   in.bias = __ldg(reinterpret_cast<const float4*>(p.dt_bias + (size_t)hv * kHeadDim + r0));
   in.beta_logit = __ldg(p.beta_logits + (size_t)t * p.HV + hv);
   return in;
+}
+
+// Start moving token t's rows (q and k of key head h, v and the raw gate of
+// value head hv) into L2 while the current chunk computes.
+__device__ __forceinline__ void prefetch_token(const DecodeArgs& p, int t, int h, int hv) {
+  prefetch_l2(p.q + ((size_t)t * p.H + h) * kHeadDim, kHeadDim * 2);
+  prefetch_l2(p.k + ((size_t)t * p.H + h) * kHeadDim, kHeadDim * 2);
+  prefetch_l2(p.v + ((size_t)t * p.HV + hv) * kHeadDim, kHeadDim * 2);
+  prefetch_l2(p.raw_gate + ((size_t)t * p.HV + hv) * kHeadDim, kHeadDim * 4);
 }
 
 // Phase 1 for one token slot: norms, gate, beta into the [token][channel]
@@ -234,20 +244,52 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
       if (half == 0) sm.eGC[c] = expf(G);
     }
     __syncthreads();
-    // ---- phase 3: the 16 x 16 products A (s < t) and Q (s <= t)
+    // ---- phase 3: the 16 x 16 products A (s < t) and Q (s <= t).  Thread
+    // (block of tokens t in {2tp, 2tp + 1} x s in {2sp, 2sp + 1}, channel
+    // phase cq) sums the 32 channels c = 4 cc + cq; the 4 phases (lanes
+    // 4k .. 4k + 3) are added with two xor-shuffles.  Blocks above the
+    // diagonal are zero.
     {
-      const int t = tid >> 4, s2 = tid & 15;
-      float a = 0.f, q = 0.f;
-      if (s2 <= t) {
+      const int cq = tid & 3, blk = tid >> 2, tp = blk >> 3, sp = blk & 7;
+      float a[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, q[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+      if (sp <= tp) {
 #pragma unroll 8
-        for (int c = 0; c < kHeadDim; ++c) {
-          const float kb = sm.kbT[c][s2];
-          a = fmaf(sm.ktT[c][t], kb, a);
-          q = fmaf(sm.qtT[c][t], kb, q);
+        for (int cc = 0; cc < kHeadDim / 4; ++cc) {
+          const int c = 4 * cc + cq;
+          const float2 kt = *reinterpret_cast<const float2*>(&sm.ktT[c][2 * tp]);
+          const float2 qt = *reinterpret_cast<const float2*>(&sm.qtT[c][2 * tp]);
+          const float2 kb = *reinterpret_cast<const float2*>(&sm.kbT[c][2 * sp]);
+          a[0][0] = fmaf(kt.x, kb.x, a[0][0]); a[0][1] = fmaf(kt.x, kb.y, a[0][1]);
+          a[1][0] = fmaf(kt.y, kb.x, a[1][0]); a[1][1] = fmaf(kt.y, kb.y, a[1][1]);
+          q[0][0] = fmaf(qt.x, kb.x, q[0][0]); q[0][1] = fmaf(qt.x, kb.y, q[0][1]);
+          q[1][0] = fmaf(qt.y, kb.x, q[1][0]); q[1][1] = fmaf(qt.y, kb.y, q[1][1]);
         }
       }
-      sm.A[t][s2] = s2 < t ? a : 0.f;
-      sm.Q[t][s2] = q;  // zero above the diagonal
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j2 = 0; j2 < 2; ++j2) {
+          a[i][j2] += __shfl_xor_sync(0xffffffffu, a[i][j2], 1);
+          a[i][j2] += __shfl_xor_sync(0xffffffffu, a[i][j2], 2);
+          q[i][j2] += __shfl_xor_sync(0xffffffffu, q[i][j2], 1);
+          q[i][j2] += __shfl_xor_sync(0xffffffffu, q[i][j2], 2);
+        }
+      if (cq == 0) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+          for (int j2 = 0; j2 < 2; ++j2) {
+            const int t = 2 * tp + i, s2 = 2 * sp + j2;
+            sm.A[t][s2] = s2 < t ? a[i][j2] : 0.f;
+            sm.Q[t][s2] = s2 <= t ? q[i][j2] : 0.f;
+          }
+      }
+    }
+    // The next chunk's token rows start moving into L2 (warp w: its slots w, w + 8).
+    if (lane == 0) {
+      const int n0 = c0 + kC;
+      if (n0 + warp < t1) prefetch_token(p, n0 + warp, h, hv);
+      if (n0 + warp + 8 < t1) prefetch_token(p, n0 + warp + 8, h, hv);
     }
     // ---- phase 4: (D_t kh_t)^T S0 and (D_t qh_t)^T S0 for the chunk
     project8(s, sm.ktT, 0, sm.ws, tl, lane);
