@@ -451,8 +451,10 @@ struct RecArgs {
 // kMulti: the n > 1 form (the token loop); both forms fit two CTAs per SM.
 template <bool kMulti>
 __global__ void __launch_bounds__(kThreads, 2) block_recurrence_kernel(const RecArgs p) {
-  __shared__ TokenStage ts;
-  __shared__ __align__(16) float zg[kHeadDim];
+  // Two record buffers: token j + 1's record and output gate are fetched while
+  // token j is stepped.
+  __shared__ TokenStage ts[2];
+  __shared__ __align__(16) float zg[2][kHeadDim];
   __shared__ __align__(16) float o_s[kHeadDim];
   __shared__ float red[kThreads / 32];
   const int bh = blockIdx.x;
@@ -465,19 +467,32 @@ __global__ void __launch_bounds__(kThreads, 2) block_recurrence_kernel(const Rec
   tile_load(s, tile, tl);  // S is not written by the preceding kernels
   pdl_wait();
   pdl_trigger();
+  // A token's record and gate as 16-byte vectors, one per thread.
   constexpr int kStageVec = (int)(sizeof(TokenStage) / sizeof(uint4));
+  constexpr int kRecVec = kStageVec + kHeadDim / 4;
+  static_assert(kRecVec <= kThreads, "one vector per thread");
+  auto fetch = [&](size_t r) -> uint4 {
+    if (tid < kStageVec) return reinterpret_cast<const uint4*>(p.stage + r * p.nh + h)[tid];
+    if (tid < kRecVec)
+      return reinterpret_cast<const uint4*>(p.zgate + (r * p.nh + h) * kHeadDim)[tid - kStageVec];
+    return make_uint4(0u, 0u, 0u, 0u);
+  };
+  auto put = [&](int buf, uint4 v) {
+    if (tid < kStageVec)
+      reinterpret_cast<uint4*>(&ts[buf])[tid] = v;
+    else if (tid < kRecVec)
+      reinterpret_cast<uint4*>(zg[buf])[tid - kStageVec] = v;
+  };
   const int n = kMulti ? p.n : 1;
+  put(0, fetch((size_t)b * n));
 #pragma unroll 1
   for (int j = 0; j < n; ++j) {
     const size_t r = (size_t)b * n + j;
-    if (j > 0) __syncthreads();  // the previous token's ts, zg and o_s are consumed
-    const uint4* src = reinterpret_cast<const uint4*>(p.stage + r * p.nh + h);
-    for (int i = tid; i < kStageVec; i += kThreads) reinterpret_cast<uint4*>(&ts)[i] = src[i];
-    if (tid < kHeadDim / 4)
-      reinterpret_cast<uint4*>(zg)[tid] =
-          reinterpret_cast<const uint4*>(p.zgate + (r * p.nh + h) * kHeadDim)[tid];
-    __syncthreads();
-    const float4 o = tile_token_step(s, ts, tl);
+    const int buf = j & 1;
+    const bool more = kMulti && j + 1 < n;
+    const uint4 next = more ? fetch(r + 1) : make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();  // record j is in place; token j - 1's o_s is consumed
+    const float4 o = tile_token_step(s, ts[buf], tl);
     if (tl.rg == 0) *reinterpret_cast<float4*>(&o_s[tl.col]) = o;
     __syncthreads();
     const float od = tid < kHeadDim ? o_s[tid] : 0.f;
@@ -485,8 +500,11 @@ __global__ void __launch_bounds__(kThreads, 2) block_recurrence_kernel(const Rec
     if (tid < kHeadDim) {
       const float inv = rsqrtf(m2 / (float)kHeadDim + p.rms_norm_eps);
       const size_t col = (size_t)h * kHeadDim + tid;  // W_o rows are head-outer
-      split_bf16(od * inv * zg[tid], p.on2 + r * p.CV + col, p.on2 + ((size_t)p.R + r) * p.CV + col);
+      split_bf16(od * inv * zg[buf][tid], p.on2 + r * p.CV + col,
+                 p.on2 + ((size_t)p.R + r) * p.CV + col);
     }
+    // The other buffer was last read by token j - 1, before this token's barriers.
+    if (more) put(buf ^ 1, next);
   }
   tile_store(tile, s, tl);
 }

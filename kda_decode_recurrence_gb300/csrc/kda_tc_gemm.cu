@@ -109,11 +109,12 @@ struct GemmShape {
   int tail_n;      // of being written per split
 };
 
-// Dynamic shared memory, 1024-aligned: the weight ring (wstages x 16 KiB A
-// tiles), the activation ring (xstages x 2*RB*128 B B tiles), then the
+// Dynamic shared memory, 1024-aligned: the weight ring (wstages x mtiles x
+// 16 KiB A tiles), the activation ring (xstages x 2*RB*128 B B tiles), then the
 // mbarriers and the TMEM base address word.  The two rings have their own
 // producers and barriers, so the weight stream (HBM) runs as far ahead as
 // its ring allows while the activation tiles (L2 hits) follow their own.
+template <int MT>  // 128-column weight tiles per CTA
 __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
     const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
     float* __restrict__ Ypart, const GemmShape sh, int32_t* __restrict__ err) {
@@ -122,21 +123,23 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * kTileN;
+  const int n0 = blockIdx.x * kTileN * MT;
   const int ks = blockIdx.y;
   const int r0 = blockIdx.z * 128;
   const int rows = min(128, sh.R - r0);
   const int RB = (rows + 31) & ~31;        // token rows per hi/lo half (32..128)
   const int NM = 2 * RB;                   // MMA N
-  const uint32_t tmem_cols = NM <= 64 ? 64 : (NM <= 128 ? 128 : 256);
+  uint32_t tmem_cols = 64;                 // a power of two >= MT accumulators of NM columns
+  while (tmem_cols < (uint32_t)(MT * NM)) tmem_cols *= 2;
   const int b_bytes = NM * 128;            // hi and lo boxes, 128 B per token row
+  const int a_bytes = kABytes * MT;        // one weight stage
   const int nW = sh.wstages, nX = sh.xstages;
   const int nkb = sh.Kdim / kBK;
   const int kb0 = (int)((long long)ks * nkb / sh.KS);
   const int kb1 = (int)((long long)(ks + 1) * nkb / sh.KS);
 
   unsigned char* wring = smem;
-  unsigned char* xring = smem + nW * kABytes;
+  unsigned char* xring = smem + nW * a_bytes;
   uint64_t* wfull = reinterpret_cast<uint64_t*>(xring + nX * b_bytes);
   uint64_t* wempty = wfull + kMaxWStages;
   uint64_t* xfull = wempty + kMaxWStages;
@@ -173,10 +176,14 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
   const int pre = min(nW, kb1 - kb0);
   if (warp == 0 && lane == 0) {
     for (int i = 0; i < pre; ++i) {
-      unsigned char* a_s = wring + i * kABytes;
-      mbar_expect_tx(&wfull[i], kABytes);
-      tma_load_2d(a_s, &tmW, &wfull[i], n0, (kb0 + i) * kBK);
-      tma_load_2d(a_s + kABytes / 2, &tmW, &wfull[i], n0 + 64, (kb0 + i) * kBK);
+      unsigned char* a_s = wring + i * a_bytes;
+      mbar_expect_tx(&wfull[i], a_bytes);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        tma_load_2d(a_s + mt * kABytes, &tmW, &wfull[i], n0 + mt * kTileN, (kb0 + i) * kBK);
+        tma_load_2d(a_s + mt * kABytes + kABytes / 2, &tmW, &wfull[i], n0 + mt * kTileN + 64,
+                    (kb0 + i) * kBK);
+      }
     }
   }
   pdl_wait();
@@ -188,10 +195,14 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
     for (int kb = kb0 + pre; kb < kb1 && ok; ++kb) {
       const int i = kb - kb0, s = i % nW, round = i / nW;
       if (!mbar_wait(&wempty[s], (round - 1) & 1)) { ok = false; break; }
-      unsigned char* a_s = wring + s * kABytes;
-      mbar_expect_tx(&wfull[s], kABytes);
-      tma_load_2d(a_s, &tmW, &wfull[s], n0, kb * kBK);
-      tma_load_2d(a_s + kABytes / 2, &tmW, &wfull[s], n0 + 64, kb * kBK);
+      unsigned char* a_s = wring + s * a_bytes;
+      mbar_expect_tx(&wfull[s], a_bytes);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        tma_load_2d(a_s + mt * kABytes, &tmW, &wfull[s], n0 + mt * kTileN, kb * kBK);
+        tma_load_2d(a_s + mt * kABytes + kABytes / 2, &tmW, &wfull[s], n0 + mt * kTileN + 64,
+                    kb * kBK);
+      }
     }
   } else if (warp == 2 && lane == 0) {
     // activation producer
@@ -216,16 +227,19 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
         break;
       }
       tc_fence_after();
-      const uint32_t a_addr = smem_u32(wring + sw * kABytes);
+      const uint32_t a_addr = smem_u32(wring + sw * a_bytes);
       const uint32_t b_addr = smem_u32(xring + sx * b_bytes);
 #pragma unroll
       for (int j = 0; j < kBK / 16; ++j) {
-        // A: MN-major, atoms of 64 columns x 8 rows; next column atom 8 KiB
-        // away (LBO), next 8-row group 1 KiB away (SBO); 16 rows per step.
-        const uint64_t adesc = smem_desc_sw128(a_addr + j * 2048, 8192, 1024);
         // B: K-major, 128-byte rows, 8-row groups 1 KiB apart; 32 B per step.
         const uint64_t bdesc = smem_desc_sw128(b_addr + j * 32, 16, 1024);
-        mma_bf16(tmem, adesc, bdesc, idesc, (kb > kb0 || j > 0) ? 1u : 0u);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          // A: MN-major, atoms of 64 columns x 8 rows; next column atom 8 KiB
+          // away (LBO), next 8-row group 1 KiB away (SBO); 16 rows per step.
+          const uint64_t adesc = smem_desc_sw128(a_addr + mt * kABytes + j * 2048, 8192, 1024);
+          mma_bf16(tmem + mt * NM, adesc, bdesc, idesc, (kb > kb0 || j > 0) ? 1u : 0u);
+        }
       }
       mma_commit(&wempty[sw]);
       mma_commit(&xempty[sx]);
@@ -241,10 +255,12 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
     if (lane == 0) atomicOr(err, KDA_DEV_TIMEOUT);
   }
   tc_fence_after();
-  const int m = n0 + warp * 32 + lane;
-  const bool to_tail = sh.tail != nullptr && n0 >= sh.tail_col;  // whole tiles
-  if (have) {
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    if (!have) break;
+    const int m = n0 + mt * kTileN + warp * 32 + lane;
+    const bool to_tail = sh.tail != nullptr && n0 + mt * kTileN >= sh.tail_col;  // whole tiles
+    const uint32_t lane_base = tmem + mt * NM + ((uint32_t)(warp * 32) << 16);
     for (int c = 0; c < RB / 32; ++c) {
       float hi[32], lo[32];
       tmem_ld_32cols(lane_base + c * 32, hi);
@@ -285,32 +301,37 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer
 
 }  // namespace
 
-// Ring depths for R token rows.  Every CTA streams its weight slice once
-// from HBM but re-reads the activations of its contraction range from L2,
-// 2*RB*128 bytes per 16 KiB weight stage, so for 32 rows (8 KiB per stage)
-// two activation stages suffice and two CTAs share an SM (113 KiB each) with
-// the deepest weight ring that fits; larger row blocks take one CTA per SM
-// (227 KiB) and four activation stages.
-static void gemm_rings(int R, int* wstages, int* xstages, size_t* smem) {
+// Ring depths and tile width for R token rows.  Every CTA streams its weight
+// slice once from HBM but re-reads the activations of its contraction range
+// from L2, 2*RB*128 bytes per 64-row stage.  For up to 32 rows (8 KiB per
+// stage) a CTA takes one 128-column weight tile, two activation stages and the
+// deepest weight ring that lets two CTAs share an SM (113 KiB each).  Larger
+// row blocks take one CTA per SM (227 KiB) with two 128-column weight tiles
+// per activation tile, which halves the activation re-reads, and 3-4
+// activation stages.
+struct GemmRings {
+  int wstages, xstages, mtiles;
+  size_t smem;
+};
+
+static GemmRings gemm_rings(int R) {
   const int rows = R < 128 ? R : 128;
   const int RB = (rows + 31) & ~31;
   const size_t b_bytes = (size_t)2 * RB * 128;
   const size_t extra = 1024 + (2 * kMaxWStages + 2 * kMaxXStages + 1) * 8 + 16;
+  GemmRings g;
+  g.mtiles = RB <= 32 ? 1 : 2;
   const size_t budget = RB <= 32 ? 113 * 1024 : 227 * 1024;
-  const int x = RB <= 32 ? 2 : kMaxXStages;
-  int w = (int)((budget - extra - x * b_bytes) / kABytes);
+  g.xstages = RB <= 32 ? 2 : (RB == 128 ? 3 : kMaxXStages);
+  const size_t a_bytes = (size_t)kABytes * g.mtiles;
+  int w = (int)((budget - extra - g.xstages * b_bytes) / a_bytes);
   if (w > kMaxWStages) w = kMaxWStages;
-  *wstages = w;
-  *xstages = x;
-  *smem = extra + x * b_bytes + (size_t)w * kABytes;
+  g.wstages = w;
+  g.smem = extra + g.xstages * b_bytes + (size_t)w * a_bytes;
+  return g;
 }
 
-size_t tc_gemm_smem_bytes(int R) {
-  int w, x;
-  size_t smem;
-  gemm_rings(R, &w, &x, &smem);
-  return smem;
-}
+size_t tc_gemm_smem_bytes(int R) { return gemm_rings(R).smem; }
 
 cudaError_t launch_tc_gemm(const kda_bf16* X2, int R, int Kdim, const kda_bf16* W, int N, int KS,
                            float* Ypart, bool accumulate, int32_t* err, cudaStream_t stream,
@@ -321,16 +342,17 @@ cudaError_t launch_tc_gemm(const kda_bf16* X2, int R, int Kdim, const kda_bf16* 
   CUtensorMap tmW, tmX;
   if (!make_map(&tmW, W, (uint64_t)N, (uint64_t)Kdim, kBK)) return cudaErrorInvalidValue;
   if (!make_map(&tmX, X2, (uint64_t)Kdim, (uint64_t)2 * R, kBoxRows)) return cudaErrorInvalidValue;
-  int wstages, xstages;
-  size_t smem;
-  gemm_rings(R, &wstages, &xstages, &smem);
-  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  const GemmRings g = gemm_rings(R);
+  void (*kernel)(CUtensorMap, CUtensorMap, float*, GemmShape, int32_t*) =
+      g.mtiles == 2 ? tc_gemm_kernel<2> : tc_gemm_kernel<1>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)g.smem);
   if (e != cudaSuccess) return e;
-  GemmShape sh{R, Kdim, N, KS, accumulate ? 1 : 0, wstages, xstages, tail, tail_col,
+  GemmShape sh{R, Kdim, N, KS, accumulate ? 1 : 0, g.wstages, g.xstages, tail, tail_col,
                N - tail_col};
-  dim3 grid((N + kTileN - 1) / kTileN, KS, (R + 127) / 128);
-  return launch(tc_gemm_kernel, grid, dim3(128), smem, stream, pdl, tmW, tmX, Ypart, sh, err);
+  const int cols = kTileN * g.mtiles;
+  dim3 grid((N + cols - 1) / cols, KS, (R + 127) / 128);
+  return launch(kernel, grid, dim3(128), g.smem, stream, pdl, tmW, tmX, Ypart, sh, err);
 }
 
 }  // namespace kda

@@ -97,3 +97,15 @@ def test_block_n_tokens_equal_n_single_token_calls():
                                rtol=1e-5, atol=1e-5)
     assert_states_close(S.numpy(), S_all.cpu().double().numpy(), "S")
     np.testing.assert_allclose(cs.numpy(), cs_all.cpu().numpy(), rtol=1e-6, atol=1e-7)
+
+
+# Row blocks of more than 32 rows: the projection GEMMs take two 128-column
+# weight tiles per CTA against each activation tile (one CTA per SM).
+@pytest.mark.parametrize("B,n,Hd,nh,Kc", [(17, 4, 256, 8, 4), (9, 7, 384, 16, 3), (33, 1, 256, 8, 2)])
+def test_block_row_blocks_over_32(B, n, Hd, nh, Kc):
+    check_block(block_inputs(B=B, n=n, Hd=Hd, nh=nh, Kc=Kc, seed=90 + B + n))
+
+
+def test_block_multi_token_full_shapes_128_rows():
+    # the full weight shapes with B = 32 requests x 4 tokens (128 rows)
+    check_block(block_inputs(B=32, n=4, seed=95))
