@@ -23,6 +23,8 @@
 // One 256-thread CTA per (request, value head); the [128, 128] state tile is
 // held in registers in the layout of kda_decode (warp w: value columns
 // 16w .. 16w + 15; lane = (row group rg, column quad cg); rows rg + 8i).
+#include <cstddef>
+
 #include "kda_async.cuh"
 #include "kda_recurrence.cuh"
 
@@ -60,25 +62,81 @@ struct ChunkIn {
   float beta_logit;
 };
 
-__device__ __forceinline__ ChunkIn fetch(const DecodeArgs& p, int t, int h, int hv, int lane) {
-  const int r0 = lane * 4;
-  ChunkIn in;
-  in.q = __ldg(reinterpret_cast<const uint2*>(p.q + ((size_t)t * p.H + h) * kHeadDim + r0));
-  in.k = __ldg(reinterpret_cast<const uint2*>(p.k + ((size_t)t * p.H + h) * kHeadDim + r0));
-  in.v = __ldg(reinterpret_cast<const uint2*>(p.v + ((size_t)t * p.HV + hv) * kHeadDim + r0));
-  in.raw = __ldg(reinterpret_cast<const float4*>(p.raw_gate + ((size_t)t * p.HV + hv) * kHeadDim + r0));
-  in.bias = __ldg(reinterpret_cast<const float4*>(p.dt_bias + (size_t)hv * kHeadDim + r0));
-  in.beta_logit = __ldg(p.beta_logits + (size_t)t * p.HV + hv);
-  return in;
+
+// A chunk's raw token inputs are copied asynchronously (cp.async) into the
+// region of qh, kh and gg, which is free from the end of phase 2 until the
+// next chunk's staging: q, k, v rows (bf16, 8-byte copies: the C ABI
+// guarantees 8-byte alignment for them), the raw gate rows (16-byte copies)
+// and beta.  Byte offsets in the region:
+constexpr int kRawQ = 0, kRawK = kC * kHeadDim * 2, kRawV = 2 * kC * kHeadDim * 2;
+constexpr int kRawG = 3 * kC * kHeadDim * 2, kRawB = kRawG + kC * kHeadDim * 4;
+constexpr int kRawBytes = kRawB + kC * 4;
+
+static_assert(kRawBytes <= 3 * kC * kHeadDim * (int)sizeof(float), "raw inputs fit in qh, kh, gg");
+static_assert(offsetof(PrefillSmem, kh) == offsetof(PrefillSmem, qh) + sizeof(float) * kC * kHeadDim &&
+                  offsetof(PrefillSmem, gg) == offsetof(PrefillSmem, kh) + sizeof(float) * kC * kHeadDim,
+              "qh, kh, gg are contiguous");
+
+__device__ __forceinline__ void cp_async(void* dst, const void* src, int bytes) {
+  if (bytes == 16)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src))
+                 : "memory");
+  else if (bytes == 8)
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src))
+                 : "memory");
+  else
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src))
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Issue the copies of tokens c0 .. c0 + 15 (those before t1): the q, k, v
+// rows in PB-byte pieces (16 when all three are 16-byte aligned, else 8),
+// the gate rows in 16-byte pieces, and the 16 betas.
+template <int PB>
+__device__ __forceinline__ void issue_raw(const DecodeArgs& p, unsigned char* raw, int c0, int t1,
+                                          int h, int hv, int tid) {
+  constexpr int kPieces = kHeadDim * 2 / PB;  // per bf16 row
+  constexpr int kQKV = 3 * kC * kPieces;
+  constexpr int kGate = kC * (kHeadDim * 4 / 16);
+  for (int i = tid; i < kQKV + kGate + kC; i += kThreads) {
+    if (i < kQKV) {
+      const int a = i / (kC * kPieces), j = i - a * (kC * kPieces), tt = j / kPieces;
+      const int part = j - tt * kPieces;
+      if (c0 + tt >= t1) continue;
+      const kda_bf16* base = a == 0 ? p.q : (a == 1 ? p.k : p.v);
+      const size_t row = a < 2 ? (size_t)(c0 + tt) * p.H + h : (size_t)(c0 + tt) * p.HV + hv;
+      cp_async(raw + a * kC * kHeadDim * 2 + tt * kHeadDim * 2 + part * PB,
+               base + row * kHeadDim + part * (PB / 2), PB);
+    } else if (i < kQKV + kGate) {
+      const int j = i - kQKV, tt = j >> 5, part = j & 31;
+      if (c0 + tt >= t1) continue;
+      cp_async(raw + kRawG + tt * kHeadDim * 4 + part * 16,
+               p.raw_gate + ((size_t)(c0 + tt) * p.HV + hv) * kHeadDim + part * 4, 16);
+    } else {
+      const int tt = i - kQKV - kGate;
+      if (c0 + tt >= t1) continue;
+      cp_async(raw + kRawB + tt * 4, p.beta_logits + (size_t)(c0 + tt) * p.HV + hv, 4);
+    }
+  }
+  cp_async_commit();
 }
 
-// Start moving token t's rows (q and k of key head h, v and the raw gate of
-// value head hv) into L2 while the current chunk computes.
-__device__ __forceinline__ void prefetch_token(const DecodeArgs& p, int t, int h, int hv) {
-  prefetch_l2(p.q + ((size_t)t * p.H + h) * kHeadDim, kHeadDim * 2);
-  prefetch_l2(p.k + ((size_t)t * p.H + h) * kHeadDim, kHeadDim * 2);
-  prefetch_l2(p.v + ((size_t)t * p.HV + hv) * kHeadDim, kHeadDim * 2);
-  prefetch_l2(p.raw_gate + ((size_t)t * p.HV + hv) * kHeadDim, kHeadDim * 4);
+
+// Token slot tt's inputs for lane `lane` (entries 4 lane .. 4 lane + 3) from the raw region.
+__device__ __forceinline__ ChunkIn read_raw(const unsigned char* raw, float4 bias, int tt, int lane) {
+  ChunkIn in;
+  in.q = *reinterpret_cast<const uint2*>(raw + kRawQ + tt * kHeadDim * 2 + lane * 8);
+  in.k = *reinterpret_cast<const uint2*>(raw + kRawK + tt * kHeadDim * 2 + lane * 8);
+  in.v = *reinterpret_cast<const uint2*>(raw + kRawV + tt * kHeadDim * 2 + lane * 8);
+  in.raw = *reinterpret_cast<const float4*>(raw + kRawG + tt * kHeadDim * 4 + lane * 16);
+  in.bias = bias;
+  in.beta_logit = *reinterpret_cast<const float*>(raw + kRawB + tt * 4);
+  return in;
 }
 
 // Phase 1 for one token slot: norms, gate, beta into the [token][channel]
@@ -172,6 +230,9 @@ __device__ __forceinline__ void project8(const float4 (&s)[16], const float (*xT
 
 // Two CTAs per SM (128 registers, ~100 KB of shared memory each) so that a
 // batch of (request, head) items twice the SM count runs in one wave.
+// kPB: the piece size of the q, k, v copies (16 when all three pointers are
+// 16-byte aligned, else 8).
+template <int kPB>
 __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeArgs p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   PrefillSmem& sm = *reinterpret_cast<PrefillSmem*>(smem_raw);
@@ -209,13 +270,19 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
   const float a_exp = expf(p.a_log[hv]);
   float* out = static_cast<float*>(p.output);
 
+  unsigned char* raw = reinterpret_cast<unsigned char*>(&sm.qh[0][0]);
+  const float4 bias = __ldg(reinterpret_cast<const float4*>(p.dt_bias + (size_t)hv * kHeadDim + lane * 4));
+  issue_raw<kPB>(p, raw, t0, t1, h, hv, tid);
   for (int c0 = t0; c0 < t1; c0 += kC) {
     const int nc = min(kC, t1 - c0);
     // ---- phase 1: stage the chunk's tokens, warp w takes slots w and w + 8
     {
+      cp_async_wait_all();
+      __syncthreads();  // every thread's copies of this chunk have landed
       ChunkIn in0 = {}, in1 = {};
-      if (warp < nc) in0 = fetch(p, c0 + warp, h, hv, lane);
-      if (warp + 8 < nc) in1 = fetch(p, c0 + warp + 8, h, hv, lane);
+      if (warp < nc) in0 = read_raw(raw, bias, warp, lane);
+      if (warp + 8 < nc) in1 = read_raw(raw, bias, warp + 8, lane);
+      __syncthreads();  // the raw region is read: staging overwrites it
       stage(p, in0, warp < nc, a_exp, sm, warp, lane);
       stage(p, in1, warp + 8 < nc, a_exp, sm, warp + 8, lane);
     }
@@ -244,6 +311,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
       if (half == 0) sm.eGC[c] = expf(G);
     }
     __syncthreads();
+    // qh, kh and gg are consumed: the next chunk's raw inputs start arriving there.
+    if (c0 + kC < t1) issue_raw<kPB>(p, raw, c0 + kC, t1, h, hv, tid);
     // ---- phase 3: the 16 x 16 products A (s < t) and Q (s <= t).  Thread
     // (block of tokens t in {2tp, 2tp + 1} x s in {2sp, 2sp + 1}, channel
     // phase cq) sums the 32 channels c = 4 cc + cq; the 4 phases (lanes
@@ -284,12 +353,6 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
             sm.Q[t][s2] = s2 <= t ? q[i][j2] : 0.f;
           }
       }
-    }
-    // The next chunk's token rows start moving into L2 (warp w: its slots w, w + 8).
-    if (lane == 0) {
-      const int n0 = c0 + kC;
-      if (n0 + warp < t1) prefetch_token(p, n0 + warp, h, hv);
-      if (n0 + warp + 8 < t1) prefetch_token(p, n0 + warp + 8, h, hv);
     }
     // ---- phase 4: (D_t kh_t)^T S0 and (D_t qh_t)^T S0 for the chunk
     project8(s, sm.ktT, 0, sm.ws, tl, lane);
@@ -357,10 +420,12 @@ cudaError_t launch_kda_prefill(const DecodeArgs& args, cudaStream_t stream) {
   const long long items = (long long)args.B * args.HV;
   if (items == 0) return cudaSuccess;
   const size_t smem = sizeof(PrefillSmem);
-  cudaError_t e = cudaFuncSetAttribute(kda_prefill_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const bool a16 = ((reinterpret_cast<uintptr_t>(args.q) | reinterpret_cast<uintptr_t>(args.k) |
+                     reinterpret_cast<uintptr_t>(args.v)) & 15) == 0;
+  void (*kernel)(DecodeArgs) = a16 ? kda_prefill_kernel<16> : kda_prefill_kernel<8>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kda_prefill_kernel<<<(unsigned)items, kThreads, smem, stream>>>(args);
+  kernel<<<(unsigned)items, kThreads, smem, stream>>>(args);
   return cudaGetLastError();
 }
 

@@ -82,3 +82,31 @@ def test_padded_and_out_of_range_slots():
     rows, slots, ref_out, ref_pool = oracle_decode_sample(inp, [0, 2])
     assert_outputs_close(o[rows], ref_out)
     assert_states_close(pool[torch.tensor(slots.astype(np.int64)).cuda()].cpu().numpy(), ref_pool)
+
+
+def test_q_k_v_at_an_8_byte_offset():
+    # The C ABI asks for 8-byte alignment of q, k, v; the chunk copies use
+    # 16-byte pieces only when all three are 16-byte aligned.  Views at an
+    # 8-byte offset take the 8-byte path and must give the same results.
+    inp = decode_inputs("varlen", B=3, H=2, HV=4, max_slots=5, lengths=(37, 16, 70), seed=124)
+    d = to_device(inp)
+    views = {}
+    for name in ("q", "k", "v"):
+        t = d[name]
+        buf = torch.empty(t.numel() + 4, dtype=t.dtype, device="cuda")
+        view = buf[4:].view(t.shape)
+        view.copy_(t)
+        assert view.data_ptr() % 16 == 8
+        views[name] = view
+    out_a, pool_a, st_a = gpu_prefill(inp)
+    out = torch.full_like(out_a, float("nan"))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda_prefill(out, views["q"], views["k"], views["v"], d["raw_gate"], d["beta_logits"],
+                d["a_log"], d["dt_bias"], d["cu_seqlens"], d["state_pool"], d["state_indices"],
+                gate_mode=inp["gate_mode"], lower_bound=inp["lower_bound"], dev_status=status)
+    torch.cuda.synchronize()
+    assert st_a == 0 and int(status.item()) == 0
+    # same arithmetic in the same order: bit-identical
+    assert torch.equal(out, out_a)
+    slots = inp["state_indices"].long().cuda()
+    assert torch.equal(d["state_pool"][slots], pool_a[slots])
