@@ -344,7 +344,10 @@ constexpr int kPrepThreads = kPrepHeads * kHeadDim;  // 1024
 // (t / 8) * nh + h0 + t % 8, so a warp reads 4 runs of 8 consecutive
 // channels.  v channels and everything per (head, d) use hl = t / 128,
 // d = t % 128 (v is head-outer, so contiguous).  Each channel's conv window
-// slides across the tokens in registers and is written back once.
+// slides across the tokens in registers and is written back once.  The work
+// that does not need the gate latents (loads, convolutions, norms, most of
+// the token record) runs before the wait for the latent kernel; the forget
+// gate and the output gate after it.
 __global__ void __launch_bounds__(kPrepThreads, 1) block_prep_kernel(const PrepArgs p) {
   __shared__ float qs_[kPrepHeads][kHeadDim];
   __shared__ float ks_[kPrepHeads][kHeadDim];
@@ -362,7 +365,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1) block_prep_kernel(const PrepA
   const int w = t >> 5;
   const int w0 = hl * (kHeadDim / 32);  // the 4 warps of head hl
 
-  // Inputs no earlier kernel of this call writes: fetched before waiting.
+  // Before waiting for the latent kernel: everything that does not need its
+  // gate latents.  The projection partial sums and the tail come from the
+  // W_in GEMM, which completed before the latent kernel (launched in plain
+  // stream order) began, and so before this kernel's CTAs were launched.
   ConvChannel chq, chk, chv;
   conv_fetch(p, b, 0, cq, chq);
   conv_fetch(p, b, 1, cq, chk);
@@ -370,8 +376,6 @@ __global__ void __launch_bounds__(kPrepThreads, 1) block_prep_kernel(const PrepA
   const float dtb = p.dt_bias[(size_t)d * p.nh + h];
   const float aexp = expf(p.A_log[h]);
   const float gam = p.gamma_o[d];
-  pdl_wait();
-  pdl_trigger();
 
 #pragma unroll 1
   for (int j = 0; j < p.n; ++j) {
@@ -387,9 +391,6 @@ __global__ void __launch_bounds__(kPrepThreads, 1) block_prep_kernel(const PrepA
       pk[ks] = on ? pr[p.CQ + cq] : 0.f;
       pv[ks] = on ? pr[2 * p.CQ + cv] : 0.f;
     }
-    const size_t gzrow = (size_t)r * (p.CQ + p.CV);
-    const float graw = p.gz[gzrow + (size_t)h * kHeadDim + d];      // W_fb head-outer
-    const float zz = p.gz[gzrow + p.CQ + (size_t)d * p.nh + h];     // W_gb channel-outer
     const float bl = p.tail[(size_t)r * p.TN + kHeadDim + h];
     float xq = pq[0], xk = pk[0], xv = pv[0];
 #pragma unroll
@@ -422,12 +423,25 @@ __global__ void __launch_bounds__(kPrepThreads, 1) block_prep_kernel(const PrepA
     const float qsc = p.scale * rsqrtf(sq + p.l2_eps);
     const float ksc = rsqrtf(sk + p.l2_eps);
     const float beta = sigmoidf_(bl);
-    const float g = p.lower_bound * sigmoidf_(aexp * (graw + dtb));
     TokenStage& st = p.stage[(size_t)r * p.nh + h];
     const float kh = kv * ksc;
-    st.row[d] = RowCoef{expf(g), kh, qv * qsc, beta * kh};
+    st.row[d].kh = kh;
+    st.row[d].qh = qv * qsc;
+    st.row[d].bkh = beta * kh;
     st.v[d] = yv;
     if (d == 0) st.bqk = beta * sqk * qsc * ksc;
+  }
+  // The gates need the latent kernel's output.
+  pdl_wait();
+  pdl_trigger();
+#pragma unroll 1
+  for (int j = 0; j < p.n; ++j) {
+    const int r = b * p.n + j;
+    const size_t gzrow = (size_t)r * (p.CQ + p.CV);
+    const float graw = p.gz[gzrow + (size_t)h * kHeadDim + d];   // W_fb head-outer
+    const float zz = p.gz[gzrow + p.CQ + (size_t)d * p.nh + h];  // W_gb channel-outer
+    p.stage[(size_t)r * p.nh + h].row[d].decay =
+        expf(p.lower_bound * sigmoidf_(aexp * (graw + dtb)));
     p.zgate[((size_t)r * p.nh + h) * kHeadDim + d] = gam * sigmoidf_(zz);
   }
   conv_save(p, chq);
