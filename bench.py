@@ -46,8 +46,8 @@ FALLBACK_HBM_GBS = 6800.0
 # profiles/), tied to the kernel sources they were taken with: when the
 # sources change the figure no longer describes the kernel and is reported
 # as null.
-NCU_TRAFFIC = {"sources_sha256": "ced644a8d7c224d051d59f591829fe6f23f6d269b76c58a74ed748e0de5843a7",
-               "bytes_per_launch": 1636103168 + 1566169600}  # read + write, grouped workload
+NCU_TRAFFIC = {"sources_sha256": "77eabfa18badebdd6987c73cf538512ba54a9ef399919adc493109302e61fcca",
+               "bytes_per_launch": 1637169408 + 1569308160}  # read + write, grouped workload
 
 
 def kernel_sources_sha() -> str:

@@ -64,6 +64,60 @@ __device__ __forceinline__ TokenIn fetch_token(const DecodeArgs& p, int t, int h
   return in;
 }
 
+// The first token of the next work item, copied asynchronously (cp.async,
+// warp 0) into a small shared buffer while the current item computes: q, k,
+// v rows in 8-byte pieces (the C ABI guarantees 8-byte alignment for them),
+// the raw gate and dt_bias rows in 16-byte pieces, beta and A_log.
+struct RawToken {
+  uint2 q[32], k[32], v[32];
+  float4 raw[32], bias[32];
+  float beta_logit, a_log;
+  float pad[2];
+};
+
+__device__ __forceinline__ void cp_async_raw(void* dst, const void* src, int bytes) {
+  if (bytes == 16)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src))
+                 : "memory");
+  else if (bytes == 8)
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src))
+                 : "memory");
+  else
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src))
+                 : "memory");
+}
+
+// Warp 0, lane `lane`: the copies of token t (key head h, value head hv).
+__device__ __forceinline__ void issue_raw_token(const DecodeArgs& p, RawToken* rt, int t, int h,
+                                                int hv, int lane) {
+  const int r0 = lane * 4;
+  cp_async_raw(&rt->q[lane], p.q + ((size_t)t * p.H + h) * kHeadDim + r0, 8);
+  cp_async_raw(&rt->k[lane], p.k + ((size_t)t * p.H + h) * kHeadDim + r0, 8);
+  cp_async_raw(&rt->v[lane], p.v + ((size_t)t * p.HV + hv) * kHeadDim + r0, 8);
+  cp_async_raw(&rt->raw[lane], p.raw_gate + ((size_t)t * p.HV + hv) * kHeadDim + r0, 16);
+  cp_async_raw(&rt->bias[lane], p.dt_bias + (size_t)hv * kHeadDim + r0, 16);
+  if (lane == 0) {
+    cp_async_raw(&rt->beta_logit, p.beta_logits + (size_t)t * p.HV + hv, 4);
+    cp_async_raw(&rt->a_log, p.a_log + hv, 4);
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ TokenIn read_raw_token(const RawToken* rt, int lane) {
+  TokenIn in;
+  in.q = rt->q[lane];
+  in.k = rt->k[lane];
+  in.v = rt->v[lane];
+  in.raw = rt->raw[lane];
+  in.bias = rt->bias[lane];
+  in.beta_logit = rt->beta_logit;
+  in.a_log = rt->a_log;
+  return in;
+}
+
 // Build the warp's token record: L2 norms (warp reductions), the scaled
 // query, the gate and decay exp(g), beta and beta * (qh . kh).
 __device__ __forceinline__ void build_stage(const DecodeArgs& p, const TokenIn& in,
@@ -156,7 +210,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
   float* ring = reinterpret_cast<float*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   TokenStage* wstage = reinterpret_cast<TokenStage*>(ring + kBufs * kHeadDim * kHeadDim);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(wstage + kWarps);
+  RawToken* rawt = reinterpret_cast<RawToken*>(wstage + kWarps);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(rawt + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -176,6 +231,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
     for (int j = 0; j < kBufs && j < nmine; ++j)
       issue_item(p, first + j * G, ring + j * kHeadDim * kHeadDim, &bars[j]);
   }
+  if (warp == 0 && nmine > 0) {
+    const Item d0 = load_item(p, first);
+    if (d0.has_tile()) issue_raw_token(p, rawt, d0.t0, d0.hv / p.G, d0.hv, lane);
+  }
   __syncthreads();
 
   int j = 0;
@@ -184,8 +243,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
     const Item d = load_item(p, first + (long long)j * G);
     const bool tile = d.has_tile();
     const int h = d.hv / p.G;
-    __syncwarp();  // the warp is done with the previous item's record
-    if (tile) build_stage(p, fetch_token(p, d.t0, h, d.hv, lane), ts, lane);
+    // The item's first-token inputs, copied by warp 0 during the previous item.
+    if (warp == 0) asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    if (tile) build_stage(p, read_raw_token(rawt, lane), ts, lane);
 
     const bool arrived = mbar_wait(&bars[buf], (uint32_t)(j / kBufs) & 1u);
     float4 s[16];
@@ -209,6 +270,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
     if (threadIdx.x == 0 && j + kBufs < nmine)
       issue_item(p, first + (long long)(j + kBufs) * G, ring + buf * kHeadDim * kHeadDim,
                  &bars[buf]);
+    // Every warp has built its record from the raw buffer: warp 0 refills it
+    // with the next item's first token.
+    if (warp == 0 && j + 1 < nmine) {
+      const Item dn = load_item(p, first + (long long)(j + 1) * G);
+      if (dn.has_tile()) issue_raw_token(p, rawt, dn.t0, dn.hv / p.G, dn.hv, lane);
+    }
 
     if (!d.range_ok) {
       if (d.hv == 0 && threadIdx.x == 0) raise_status(p.dev_status, KDA_DEV_BAD_SEQLEN);
@@ -278,7 +345,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
 }  // namespace
 
 size_t decode_smem_bytes() {
-  return 128 + (size_t)kBufs * kTileBytes + kWarps * sizeof(TokenStage) + kBufs * sizeof(uint64_t);
+  return 128 + (size_t)kBufs * kTileBytes + kWarps * sizeof(TokenStage) + sizeof(RawToken) +
+         kBufs * sizeof(uint64_t);
 }
 
 cudaError_t launch_kda_decode(const DecodeArgs& args, cudaStream_t stream) {
