@@ -46,8 +46,8 @@ FALLBACK_HBM_GBS = 6800.0
 # profiles/), tied to the kernel sources they were taken with: when the
 # sources change the figure no longer describes the kernel and is reported
 # as null.
-NCU_TRAFFIC = {"sources_sha256": "77eabfa18badebdd6987c73cf538512ba54a9ef399919adc493109302e61fcca",
-               "bytes_per_launch": 1637169408 + 1569308160}  # read + write, grouped workload
+NCU_TRAFFIC = {"sources_sha256": "50e52c8472fa9e81d053e2c76f2bd733e8bebb8466d0944557b24224b3072f22",
+               "bytes_per_launch": 1637329152 + 1569918208}  # read + write, grouped workload
 
 
 def kernel_sources_sha() -> str:

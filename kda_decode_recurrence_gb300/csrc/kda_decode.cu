@@ -91,8 +91,10 @@ __device__ __forceinline__ void cp_async_raw(void* dst, const void* src, int byt
 }
 
 // Warp 0, lane `lane`: the copies of token t (key head h, value head hv).
-__device__ __forceinline__ void issue_raw_token(const DecodeArgs& p, RawToken* rt, int t, int h,
-                                                int hv, int lane) {
+// Each lane's copies arrive on `bar` (initialised for 32 arrivals) when they
+// complete, so the other warps wait for the data, not for warp 0.
+__device__ __forceinline__ void issue_raw_token(const DecodeArgs& p, RawToken* rt, uint64_t* bar,
+                                                int t, int h, int hv, int lane) {
   const int r0 = lane * 4;
   cp_async_raw(&rt->q[lane], p.q + ((size_t)t * p.H + h) * kHeadDim + r0, 8);
   cp_async_raw(&rt->k[lane], p.k + ((size_t)t * p.H + h) * kHeadDim + r0, 8);
@@ -103,7 +105,8 @@ __device__ __forceinline__ void issue_raw_token(const DecodeArgs& p, RawToken* r
     cp_async_raw(&rt->beta_logit, p.beta_logits + (size_t)t * p.HV + hv, 4);
     cp_async_raw(&rt->a_log, p.a_log + hv, 4);
   }
-  asm volatile("cp.async.commit_group;" ::: "memory");
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
 }
 
 __device__ __forceinline__ TokenIn read_raw_token(const RawToken* rt, int lane) {
@@ -212,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
   TokenStage* wstage = reinterpret_cast<TokenStage*>(ring + kBufs * kHeadDim * kHeadDim);
   RawToken* rawt = reinterpret_cast<RawToken*>(wstage + kWarps);
   uint64_t* bars = reinterpret_cast<uint64_t*>(rawt + 1);
+  uint64_t* rawbar = bars + kBufs;  // the first-token copies (32 arrivals: warp 0's lanes)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -227,15 +231,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
     raise_status(p.dev_status, KDA_DEV_BAD_SEQLEN);
   if (threadIdx.x == 0) {
     for (int i = 0; i < kBufs; ++i) mbar_init(&bars[i], 1);
+    mbar_init(rawbar, 32);
     mbar_fence_init();
     for (int j = 0; j < kBufs && j < nmine; ++j)
       issue_item(p, first + j * G, ring + j * kHeadDim * kHeadDim, &bars[j]);
   }
+  __syncthreads();  // the barriers are initialised
   if (warp == 0 && nmine > 0) {
     const Item d0 = load_item(p, first);
-    if (d0.has_tile()) issue_raw_token(p, rawt, d0.t0, d0.hv / p.G, d0.hv, lane);
+    if (d0.has_tile()) issue_raw_token(p, rawt, rawbar, d0.t0, d0.hv / p.G, d0.hv, lane);
   }
-  __syncthreads();
+  uint32_t rawphase = 0;  // fills of the first-token buffer consumed so far
 
   int j = 0;
   for (; j < nmine; ++j) {
@@ -244,9 +250,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
     const bool tile = d.has_tile();
     const int h = d.hv / p.G;
     // The item's first-token inputs, copied by warp 0 during the previous item.
-    if (warp == 0) asm volatile("cp.async.wait_all;" ::: "memory");
-    __syncthreads();
-    if (tile) build_stage(p, read_raw_token(rawt, lane), ts, lane);
+    __syncwarp();  // the warp is done with the previous item's record
+    bool raw_ok = true;
+    if (tile) {
+      raw_ok = mbar_wait(rawbar, rawphase & 1u);
+      ++rawphase;
+      build_stage(p, read_raw_token(rawt, lane), ts, lane);
+    }
 
     const bool arrived = mbar_wait(&bars[buf], (uint32_t)(j / kBufs) & 1u);
     float4 s[16];
@@ -265,8 +275,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
           s[i] = *reinterpret_cast<const float4*>(src + (tl.rg + 8 * i) * kHeadDim + tl.col);
       }
     }
-    // Every thread has read the slot: it can take the tile of item j + kBufs.
-    if (__syncthreads_or(!arrived)) break;
+    // Every thread has read the slot (and built its record from the
+    // first-token buffer): the slot takes the tile of item j + kBufs, the
+    // buffer the next item's first token.
+    if (__syncthreads_or(!arrived || !raw_ok)) break;
     if (threadIdx.x == 0 && j + kBufs < nmine)
       issue_item(p, first + (long long)(j + kBufs) * G, ring + buf * kHeadDim * kHeadDim,
                  &bars[buf]);
@@ -274,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
     // with the next item's first token.
     if (warp == 0 && j + 1 < nmine) {
       const Item dn = load_item(p, first + (long long)(j + 1) * G);
-      if (dn.has_tile()) issue_raw_token(p, rawt, dn.t0, dn.hv / p.G, dn.hv, lane);
+      if (dn.has_tile()) issue_raw_token(p, rawt, rawbar, dn.t0, dn.hv / p.G, dn.hv, lane);
     }
 
     if (!d.range_ok) {
@@ -337,6 +349,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
       raise_status(p.dev_status, KDA_DEV_TIMEOUT);
       for (int k = j; k < j + kBufs && k < nmine; ++k)
         mbar_wait(&bars[k % kBufs], (uint32_t)(k / kBufs) & 1u);
+      if (rawphase > 0) mbar_wait(rawbar, (rawphase - 1) & 1u);  // the last first-token fill
     }
     __syncthreads();
   }
@@ -346,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
 
 size_t decode_smem_bytes() {
   return 128 + (size_t)kBufs * kTileBytes + kWarps * sizeof(TokenStage) + sizeof(RawToken) +
-         kBufs * sizeof(uint64_t);
+         (kBufs + 1) * sizeof(uint64_t);
 }
 
 cudaError_t launch_kda_decode(const DecodeArgs& args, cudaStream_t stream) {
