@@ -26,6 +26,10 @@
 //                   bf16 hi/lo on2
 //   6. out GEMM     tcgen05, out += on[:, split ks] . W_o[split ks, :] for each
 //                   split (fp32 atomics into the rows the RMSNorm kernel zeroed)
+// Kernels 2, 4, 5 and 6 are programmatic dependents of the kernel before them
+// (each requests what does not depend on it -- weights, state tiles, conv
+// windows -- before waiting); the latent kernel is launched in plain stream
+// order so that its CTAs spread over every SM.
 // Intermediates live in the caller's workspace (a few MB: L2-resident).
 #include "kda_recurrence.cuh"
 #include "kda_launch.h"

@@ -21,10 +21,14 @@
 //     rows rg, rg + 8, ..., rg + 120 of its four columns (16 float4);
 //   * the k- and q-contractions over the 128 key rows are in-thread sums over
 //     16 rows followed by three xor-shuffles across the 8 row groups;
-//   * each warp prepares its own copy of the first token's vectors (normalised
-//     q and k, exp(g), beta * k, v, beta * q.k) in a private shared-memory
-//     record while the tile is in flight; later tokens of an item are staged
-//     8 at a time, one warp per token, between two CTA barriers;
+//   * the first token's raw inputs (q, k, v, gate, dt_bias, beta, A_log) of
+//     the next item are copied by warp 0 with cp.async into a small shared
+//     buffer while the current item computes; the copies complete on an
+//     mbarrier, and each warp then builds its own copy of the token's vectors
+//     (normalised q and k, exp(g), beta * k, v, beta * q.k) in a private
+//     shared-memory record while the tile is in flight; later tokens of an
+//     item are staged 8 at a time, one warp per token, between two CTA
+//     barriers;
 //   * the advanced tile is written back from registers with 128-bit
 //     streaming stores.
 //

@@ -15,12 +15,14 @@
 // Mapping (swap-AB): MMA M = 128 weight columns (A = W^T tile, MN-major in
 // shared memory), MMA N = the hi and lo copies of up to 128 tokens (B = X2
 // tile, K-major), MMA K = 16 per instruction, 64 per pipeline stage.  The
-// accumulator D[128, N] lives in TMEM.  One CTA per (128-column tile,
-// contraction split, 128-token block); 4 warps: warp 0 allocates TMEM and
-// its lane 0 issues the TMA loads, warp 1 lane 0 issues the MMAs, then all
-// four warps drain TMEM (warp w owns TMEM lanes 32w..32w+31) and write the
-// split's partial sums.  Every wait on an mbarrier is bounded by a 1 s
-// timer; on expiry the CTA records an error bit and returns cleanly.
+// accumulator D[128, N] lives in TMEM.  One CTA per (one or two 128-column
+// tiles, contraction split, 128-token block); with two tiles both
+// accumulators share each activation tile.  4 warps: warp 0 allocates TMEM
+// and its lane 0 issues the weight loads (the weight ring, from HBM), warp 2
+// lane 0 the activation loads (their own ring, L2 hits), warp 1 lane 0 the
+// MMAs; then all four warps drain TMEM (warp w owns TMEM lanes 32w..32w+31)
+// and write the split's partial sums.  Every wait on an mbarrier is bounded
+// by a 1 s timer; on expiry the CTA records an error bit and returns cleanly.
 #include <cuda.h>
 
 #include "kda_async.cuh"
