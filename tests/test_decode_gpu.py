@@ -236,3 +236,31 @@ def test_v_first_bf16_full_size_against_oracle():
     err = np.abs(got - ref_out)
     assert np.all(err <= 1e-3 * (1 + np.abs(ref_out)) + 2.0 ** -8 * np.abs(ref_out))
     assert_states_close(pool[torch.from_numpy(slots.astype(np.int64)).cuda()].cpu().numpy(), ref_pool)
+
+
+def test_pool_larger_than_4_gib():
+    # 4096 slots x 96 heads x 64 KiB = 25.8 GB: tile byte offsets far beyond
+    # 32 bits.  Only the touched slots (and neighbours used as sentinels) are
+    # filled; the oracle runs on a compact pool holding the same tiles.
+    small = decode_inputs("grouped", B=4, max_slots=4, seed=130)
+    big_slot = torch.tensor([0, 1234, 4094, 4095])
+    d = to_device(small)
+    pool = torch.empty((4096, small["HV"], 128, 128), dtype=torch.float32, device="cuda")
+    pool[big_slot.cuda()] = d["state_pool"]
+    sentinels = torch.tensor([1, 1233, 1235, 4093]).cuda()
+    pool[sentinels] = 7.0
+    idx = big_slot[small["state_indices"].long()].to(torch.int32).cuda()
+    out = torch.full((small["T"], small["HV"], small["V"]), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda_decode(out, d["q"], d["k"], d["v"], d["raw_gate"], d["beta_logits"], d["a_log"],
+               d["dt_bias"], d["cu_seqlens"], pool, idx, gate_mode=small["gate_mode"],
+               lower_bound=small["lower_bound"], dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    rows, slots, ref_out, ref_pool = oracle_decode_sample(small, range(small["B"]))
+    assert_outputs_close(out[torch.from_numpy(rows).cuda()].cpu().numpy(), ref_out)
+    got = pool[big_slot[torch.from_numpy(slots.astype(np.int64))].cuda()].cpu().numpy()
+    assert_states_close(got, ref_pool)
+    assert bool((pool[sentinels] == 7.0).all())
+    del pool
+    torch.cuda.empty_cache()
