@@ -35,6 +35,8 @@
 // The read uses q^T S_new = q^T (D S) + beta (q.k) u with u = v - k^T (D S),
 // which is the same quantity as reading after the write, with one pass over
 // the tile per token instead of two.
+#include <type_traits>
+
 #include "kda_async.cuh"
 #include "kda_recurrence.cuh"
 
@@ -126,9 +128,11 @@ __device__ __forceinline__ TokenIn read_raw_token(const RawToken* rt, int lane) 
 }
 
 // Build the warp's token record: L2 norms (warp reductions), the scaled
-// query, the gate and decay exp(g), beta and beta * (qh . kh).
-__device__ __forceinline__ void build_stage(const DecodeArgs& p, const TokenIn& in,
-                                            TokenStage& ts, int lane) {
+// query, the gate and decay exp(g), beta and beta * (qh . kh).  Stage is
+// TokenStage (row-major tiles) or TokenStageT (transposed tiles).
+template <class Stage>
+__device__ __forceinline__ void build_stage(const DecodeArgs& p, const TokenIn& in, Stage& ts,
+                                            int lane) {
   const int r0 = lane * 4;
   const float q[4] = {bf16_lo(in.q.x), bf16_hi(in.q.x), bf16_lo(in.q.y), bf16_hi(in.q.y)};
   const float k[4] = {bf16_lo(in.k.x), bf16_hi(in.k.x), bf16_lo(in.k.y), bf16_hi(in.k.y)};
@@ -148,12 +152,27 @@ __device__ __forceinline__ void build_stage(const DecodeArgs& p, const TokenIn& 
   const float a_exp = expf(in.a_log);
   const float xr[4] = {in.raw.x + in.bias.x, in.raw.y + in.bias.y, in.raw.z + in.bias.z,
                        in.raw.w + in.bias.w};
+  if constexpr (std::is_same<Stage, TokenStageT>::value) {
+    float dec[4], kh[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float g = (p.gate_mode == KDA_GATE_SOFTPLUS) ? -a_exp * softplusf_(xr[i])
-                                                        : p.lower_bound * sigmoidf_(a_exp * xr[i]);
-    const float kh = k[i] * ks;
-    ts.row[r0 + i] = RowCoef{expf(g), kh, q[i] * qs, beta * kh};
+    for (int i = 0; i < 4; ++i) {
+      const float g = (p.gate_mode == KDA_GATE_SOFTPLUS) ? -a_exp * softplusf_(xr[i])
+                                                          : p.lower_bound * sigmoidf_(a_exp * xr[i]);
+      dec[i] = expf(g);
+      kh[i] = k[i] * ks;
+    }
+    ts.decay[lane] = make_float4(dec[0], dec[1], dec[2], dec[3]);
+    ts.kh[lane] = make_float4(kh[0], kh[1], kh[2], kh[3]);
+    ts.qh[lane] = make_float4(q[0] * qs, q[1] * qs, q[2] * qs, q[3] * qs);
+    ts.bkh[lane] = make_float4(beta * kh[0], beta * kh[1], beta * kh[2], beta * kh[3]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float g = (p.gate_mode == KDA_GATE_SOFTPLUS) ? -a_exp * softplusf_(xr[i])
+                                                          : p.lower_bound * sigmoidf_(a_exp * xr[i]);
+      const float kh = k[i] * ks;
+      ts.row[r0 + i] = RowCoef{expf(g), kh, q[i] * qs, beta * kh};
+    }
   }
   *reinterpret_cast<float4*>(&ts.v[r0]) =
       make_float4(bf16_lo(in.v.x), bf16_hi(in.v.x), bf16_lo(in.v.y), bf16_hi(in.v.y));
@@ -192,6 +211,15 @@ __device__ __forceinline__ void issue_item(const DecodeArgs& p, long long item, 
   if (copy) bulk_load(dst, tile_ptr(p, d), kTileBytes, bar);
 }
 
+__device__ __forceinline__ float4 step(float4 (&s)[16], const TokenStage& ts, TileLane tl,
+                                       TileLaneT) {
+  return tile_token_step(s, ts, tl);
+}
+__device__ __forceinline__ float4 step(float4 (&s)[16], const TokenStageT& ts, TileLane,
+                                       TileLaneT tlt) {
+  return tile_t_token_step(s, ts, tlt);
+}
+
 // Output row of token t, value head hv: 4 consecutive values from column col.
 template <bool kOutBf16>
 __device__ __forceinline__ void store_out(const DecodeArgs& p, int t, int hv, int col, float4 o) {
@@ -209,14 +237,16 @@ __device__ __forceinline__ void store_out(const DecodeArgs& p, int t, int hv, in
 }
 
 // kVFirst: tiles are stored [V, K] (row v contiguous over k, the layout of a
-// transposed state); the register tile is still S[k][v], so the element
-// (k, v) is read from and written to v * 128 + k.
+// transposed state); the lanes then hold runs of 4 rows of one column
+// (TileLaneT, tile_t_token_step), so tile loads and stores stay 128-bit and
+// conflict-free.
 template <bool kVFirst, bool kOutBf16>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const DecodeArgs p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   float* ring = reinterpret_cast<float*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  TokenStage* wstage = reinterpret_cast<TokenStage*>(ring + kBufs * kHeadDim * kHeadDim);
+  using Stage = typename std::conditional<kVFirst, TokenStageT, TokenStage>::type;
+  Stage* wstage = reinterpret_cast<Stage*>(ring + kBufs * kHeadDim * kHeadDim);
   RawToken* rawt = reinterpret_cast<RawToken*>(wstage + kWarps);
   uint64_t* bars = reinterpret_cast<uint64_t*>(rawt + 1);
   uint64_t* rawbar = bars + kBufs;  // the first-token copies (32 arrivals: warp 0's lanes)
@@ -224,7 +254,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const TileLane tl = tile_lane();
-  TokenStage& ts = wstage[warp];
+  const TileLaneT tlt = tile_lane_t();
+  Stage& ts = wstage[warp];
   const long long items = (long long)p.B * p.HV;
   const long long G = gridDim.x;
   const long long first = blockIdx.x;
@@ -266,13 +297,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
     float4 s[16];
     if (tile && arrived) {
       const float* src = ring + buf * kHeadDim * kHeadDim;
-      if (kVFirst) {
+      if constexpr (kVFirst) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int r = tl.rg + 8 * i;
-          s[i] = make_float4(src[(tl.col + 0) * kHeadDim + r], src[(tl.col + 1) * kHeadDim + r],
-                             src[(tl.col + 2) * kHeadDim + r], src[(tl.col + 3) * kHeadDim + r]);
-        }
+        for (int m = 0; m < 4; ++m)
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            s[4 * m + c] = *reinterpret_cast<const float4*>(src + tile_t_offset(tlt, m, c));
       } else {
 #pragma unroll
         for (int i = 0; i < 16; ++i)
@@ -311,8 +341,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
     // First token: this warp's own record, built while the tile was in flight.
     __syncwarp();
     {
-      const float4 o = tile_token_step(s, ts, tl);
-      if (tl.rg == 0) store_out<kOutBf16>(p, d.t0, d.hv, tl.col, o);
+      const float4 o = step(s, ts, tl, tlt);
+      if (kVFirst ? tlt.kq == 0 : tl.rg == 0)
+        store_out<kOutBf16>(p, d.t0, d.hv, kVFirst ? tlt.col : tl.col, o);
     }
     // Later tokens, 8 per round: warp w stages token c0 + w into record w, then
     // every warp steps through the round's records.  (Uniform across the CTA:
@@ -323,24 +354,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
       if (warp < nc) build_stage(p, fetch_token(p, c0 + warp, h, d.hv, lane), wstage[warp], lane);
       __syncthreads();
       for (int jj = 0; jj < nc; ++jj) {
-        const float4 o = tile_token_step(s, wstage[jj], tl);
-        if (tl.rg == 0) store_out<kOutBf16>(p, c0 + jj, d.hv, tl.col, o);
+        const float4 o = step(s, wstage[jj], tl, tlt);
+        if (kVFirst ? tlt.kq == 0 : tl.rg == 0)
+          store_out<kOutBf16>(p, c0 + jj, d.hv, kVFirst ? tlt.col : tl.col, o);
       }
     }
     // The next item's first record goes into wstage[warp]: wait until every
     // warp has finished reading this item's rounds.
     if (d.t1 - d.t0 > 1) __syncthreads();
     float* dst = tile_ptr(p, d);
-    if (kVFirst) {
-      // Each instruction writes 4 runs of 8 consecutive floats (full sectors).
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int r = tl.rg + 8 * i;
-        __stcs(dst + (tl.col + 0) * kHeadDim + r, s[i].x);
-        __stcs(dst + (tl.col + 1) * kHeadDim + r, s[i].y);
-        __stcs(dst + (tl.col + 2) * kHeadDim + r, s[i].z);
-        __stcs(dst + (tl.col + 3) * kHeadDim + r, s[i].w);
-      }
+    if constexpr (kVFirst) {
+      tile_t_store(dst, s, tlt);
     } else {
       tile_store(dst, s, tl);
     }
