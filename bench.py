@@ -46,8 +46,8 @@ FALLBACK_HBM_GBS = 6800.0
 # profiles/), tied to the kernel sources they were taken with: when the
 # sources change the figure no longer describes the kernel and is reported
 # as null.
-NCU_TRAFFIC = {"sources_sha256": "cacfb58ad403fd9ec821474ae456492caed7b31fbe58b599355525ec9c79c22d",
-               "bytes_per_launch": 1637329152 + 1569918208}  # read + write, grouped workload
+NCU_TRAFFIC = {"sources_sha256": "39cc73d1d4d3d48bdb271258060f50059e6652b7c466ec632d1e0a7105f800ec",
+               "bytes_per_launch": 1637349888 + 1569355776}  # read + write, grouped workload
 
 
 def kernel_sources_sha() -> str:
@@ -575,9 +575,10 @@ def run_gpu(args, rank, world, local):
 def run_profile_case(args, which: str):
     """A reduced case for ncu captures: the decode kernel on B = 32 requests x
     1 token, H = 48, HV = 96 (a 64-slot, 400 MB pool; 200 MB of state traffic
-    per launch, above the L2 size), or the block at its full size.  Prints
-    the median kernel time only."""
-    from kda_decode_recurrence_gb300 import kda_decode
+    per launch, above the L2 size), with K-first tiles ("decode") or V-first
+    tiles ("decode_vfirst", fp32 output), or the block at its full size.
+    Prints the median kernel time only."""
+    from kda_decode_recurrence_gb300 import STATE_V_FIRST, kda_decode_ex
     dev = torch.device("cuda", 0)
     if which == "block":
         print(json.dumps({"profile": "block", **run_block(args.steps, args.warmup)}))
@@ -592,22 +593,23 @@ def run_profile_case(args, which: str):
     for i in range(args.warmup + args.steps):
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record()
-        kda_decode(out, d["q"], d["k"], d["v"], d["raw_gate"], d["beta_logits"], d["a_log"],
-                   d["dt_bias"], d["cu_seqlens"], d["state_pool"], d["state_indices"],
-                   gate_mode=inp["gate_mode"], lower_bound=inp["lower_bound"])
+        kda_decode_ex(out, d["q"], d["k"], d["v"], d["raw_gate"], d["beta_logits"], d["a_log"],
+                      d["dt_bias"], d["cu_seqlens"], d["state_pool"], d["state_indices"],
+                      gate_mode=inp["gate_mode"], lower_bound=inp["lower_bound"],
+                      state_layout=STATE_V_FIRST if which == "decode_vfirst" else 0)
         e.record()
         e.synchronize()
         if i >= args.warmup:
             times.append(s.elapsed_time(e) * 1e-3)
     t = statistics.median(times)
     nbytes = decode_bytes(inp["B"], inp["T"], inp["H"], inp["HV"], inp["K"], inp["V"])
-    print(json.dumps({"profile": "decode", "B": inp["B"], "us": t * 1e6,
+    print(json.dumps({"profile": which, "B": inp["B"], "us": t * 1e6,
                       "algorithmic_bytes": nbytes, "gbs": nbytes / t / 1e9}))
 
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile", choices=["decode", "block", "prefill"], default=None,
+    ap.add_argument("--profile", choices=["decode", "decode_vfirst", "block", "prefill"], default=None,
                     help="run a reduced case of one kernel for ncu (no JSON bench line)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)

@@ -30,7 +30,11 @@
 //     item are staged 8 at a time, one warp per token, between two CTA
 //     barriers;
 //   * the advanced tile is written back from registers with 128-bit
-//     streaming stores.
+//     streaming stores;
+//   * transposed (V-first) tiles keep the same warp-to-column split, but each
+//     lane holds runs of 4 consecutive rows of its columns (the tile is
+//     contiguous along k there), with the token record laid out by field, so
+//     their loads and stores stay 128-bit and bank-conflict-free too.
 //
 // The read uses q^T S_new = q^T (D S) + beta (q.k) u with u = v - k^T (D S),
 // which is the same quantity as reading after the write, with one pass over
