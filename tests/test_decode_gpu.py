@@ -156,6 +156,60 @@ def test_lower_bound_gate_never_amplifies_on_gpu():
     assert np.all(ratio <= 1.0) and np.all(ratio >= np.exp(-5.0) * (1 - 1e-6))
 
 
+def test_beta_zero_scales_each_state_row_and_nothing_else():
+    # beta == 0 (sigmoid(-200) is 0 in fp32): the step is the decay alone, so
+    # every row k of the advanced tile is the old row times one factor exp(g_k)
+    # (one fp32 rounding per element), and that factor is the oracle's.
+    inp = decode_inputs("varlen", B=6, H=2, HV=4, max_slots=8, lengths=(1,) * 6, seed=55)
+    inp["beta_logits"] = torch.full_like(inp["beta_logits"], -200.0)
+    out, pool, st = gpu_decode(inp)
+    assert st == 0
+    slots = inp["state_indices"].long()
+    before = to_f64(inp["state_pool"][slots])
+    after = pool[slots.cuda()].cpu().double().numpy()
+    ratio = after / before                                   # [B, HV, K, V]
+    row = np.median(ratio, axis=-1, keepdims=True)
+    assert np.all(np.abs(ratio - row) <= 2.0 ** -22 * np.abs(row))
+    rows, _, ref_out, ref_pool = oracle_decode_sample(inp, range(inp["B"]))
+    ref_ratio = ref_pool[..., :1] / before[..., :1]
+    np.testing.assert_allclose(row, ref_ratio, rtol=1e-4)
+    assert_outputs_close(out.cpu().numpy()[rows], ref_out)
+
+
+def test_grouped_heads_equal_duplicated_heads_bit_for_bit():
+    # G = 2 (H = 48 key heads for HV = 96 value heads) is the same computation
+    # as H = 96 with each key head's q and k repeated for its two value heads.
+    inp = decode_inputs("grouped")
+    out_g, pool_g, st_g = gpu_decode(inp)
+    dup = dict(inp)
+    dup["q"] = inp["q"].repeat_interleave(2, dim=1).contiguous()
+    dup["k"] = inp["k"].repeat_interleave(2, dim=1).contiguous()
+    out_d, pool_d, st_d = gpu_decode(dup)
+    assert st_g == 0 and st_d == 0
+    assert torch.equal(out_g, out_d)
+    assert torch.equal(pool_g, pool_d)
+
+
+def test_permuting_requests_with_their_slots_permutes_the_outputs():
+    lengths = (3, 1, 5, 2, 4, 1, 9)
+    inp = decode_inputs("varlen", B=7, H=2, HV=4, max_slots=10, lengths=lengths, seed=56)
+    out, pool, st = gpu_decode(inp)
+    assert st == 0
+    perm = [4, 0, 6, 2, 5, 1, 3]
+    cu = inp["cu_seqlens"].tolist()
+    rows = torch.cat([torch.arange(cu[b], cu[b + 1]) for b in perm])
+    new_len = [lengths[b] for b in perm]
+    moved = dict(inp)
+    for key in ("q", "k", "v", "raw_gate", "beta_logits"):
+        moved[key] = inp[key][rows].contiguous()
+    moved["cu_seqlens"] = torch.tensor(np.concatenate([[0], np.cumsum(new_len)]), dtype=torch.int32)
+    moved["state_indices"] = inp["state_indices"][perm].contiguous()
+    out_p, pool_p, st_p = gpu_decode(moved)
+    assert st_p == 0
+    assert torch.equal(out_p, out[rows.cuda()])
+    assert torch.equal(pool_p, pool)
+
+
 def test_persistent_ring_with_mixed_items():
     # Many more (request, head) items than SMs, so every CTA cycles through its
     # copy ring many times, with padded, out-of-range and empty requests mixed
