@@ -14,7 +14,9 @@
 //   2. proj GEMM    tcgen05, P_part[ks] = x[:, split ks] . W_in[split ks, :]   [KS1, R, I]
 //                   (split-K so every SM streams a slice of the 103 MB W_in;
 //                   consumers add the KS1 partial sums of q, k, v; the g_a,
-//                   beta, f_a columns are summed in place into `tail`)
+//                   beta, f_a columns are summed in place into `tail`); as
+//                   its CTAs finish they bring conv_state, W_fb and W_gb
+//                   into L2 for kernels 3 and 4
 //   3. latent       graw = f_a . W_fb, z = g_a . W_gb (CUDA cores)            [R, CQ + CV]
 //   4. prep         one CTA per (b, 8 heads), channels read coalesced: short
 //                   conv + SiLU + conv_state update of the q, k, v channels,
@@ -555,8 +557,13 @@ cudaError_t launch_kda_block(const BlockArgs& a, cudaStream_t stream) {
   // g_a, beta and f_a (the last TN columns) are summed over the splits in
   // place (into `tail`, zeroed by the RMSNorm kernel): every latent CTA reads
   // the f_a / g_a panel, so it is kept at one copy.
+  // As their MMAs finish, the W_in CTAs bring into L2 what the next two
+  // kernels read first: conv_state (prep) and the gate latent weights.
+  const L2Prefetch pf{{a.conv_state, a.W_fb, a.W_gb},
+                      {(size_t)a.B * 3 * L.CQ * (a.Kc - 1) * sizeof(float),
+                       (size_t)a.K * L.CQ * sizeof(kda_bf16), (size_t)a.K * L.CV * sizeof(kda_bf16)}};
   e = launch_tc_gemm(reinterpret_cast<const kda_bf16*>(x2), L.R, a.Hd, a.W_in, L.I, L.KS1, ppart,
-                     false, err, stream, true, tail, L.TC);
+                     false, err, stream, true, tail, L.TC, &pf);
   if (e != cudaSuccess) return e;
   // Within the tail: g_a at 0, beta at K, f_a at K + nh.
   const int off_ga = 0;

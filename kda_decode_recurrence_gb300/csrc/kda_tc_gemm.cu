@@ -21,7 +21,8 @@
 // and its lane 0 issues the weight loads (the weight ring, from HBM), warp 2
 // lane 0 the activation loads (their own ring, L2 hits), warp 1 lane 0 the
 // MMAs; then all four warps drain TMEM (warp w owns TMEM lanes 32w..32w+31)
-// and write the split's partial sums.  Every wait on an mbarrier is bounded
+// and write the split's partial sums; warp 3 lane 0 first issues this CTA's
+// slice of the optional L2 prefetch ranges.  Every wait on an mbarrier is bounded
 // by a 1 s timer; on expiry the CTA records an error bit and returns cleanly.
 #include <cuda.h>
 
@@ -109,6 +110,7 @@ struct GemmShape {
   float* tail;     // optional: columns >= tail_col are added (fp32 atomics)
   int tail_col;    // into tail[r][n - tail_col] (row stride tail_n) instead
   int tail_n;      // of being written per split
+  L2Prefetch pf;   // ranges to bring into L2 after the MMAs (bytes 0: none)
 };
 
 // Dynamic shared memory, 1024-aligned: the weight ring (wstages x mtiles x
@@ -256,6 +258,23 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
   if (!have || !ok) {
     if (lane == 0) atomicOr(err, KDA_DEV_TIMEOUT);
   }
+  if (have && warp == 3 && lane == 0) {
+    // This CTA's slice of each prefetch range (16-byte pieces).
+    const size_t ctas = (size_t)gridDim.x * gridDim.y * gridDim.z;
+    const size_t cta = ((size_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+#pragma unroll
+    for (int r = 0; r < 3; ++r) {
+      const size_t nb = sh.pf.bytes[r] & ~(size_t)15;
+      if (nb == 0) continue;
+      const size_t share = ((nb + ctas - 1) / ctas + 15) & ~(size_t)15;
+      const size_t lo = min(cta * share, nb), hi = min(lo + share, nb);
+      if (hi > lo)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                         static_cast<const char*>(sh.pf.ptr[r]) + lo),
+                     "r"((uint32_t)(hi - lo))
+                     : "memory");
+    }
+  }
   tc_fence_after();
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
@@ -337,7 +356,7 @@ size_t tc_gemm_smem_bytes(int R) { return gemm_rings(R).smem; }
 
 cudaError_t launch_tc_gemm(const kda_bf16* X2, int R, int Kdim, const kda_bf16* W, int N, int KS,
                            float* Ypart, bool accumulate, int32_t* err, cudaStream_t stream,
-                           bool pdl, float* tail, int tail_col) {
+                           bool pdl, float* tail, int tail_col, const L2Prefetch* prefetch) {
   if (R < 1 || Kdim % kBK != 0 || N % 8 != 0 || KS < 1 || KS > Kdim / kBK ||
       (tail && (tail_col % kTileN != 0 || tail_col < 0 || tail_col >= N)))
     return cudaErrorInvalidValue;
@@ -351,7 +370,13 @@ cudaError_t launch_tc_gemm(const kda_bf16* X2, int R, int Kdim, const kda_bf16* 
                                        (int)g.smem);
   if (e != cudaSuccess) return e;
   GemmShape sh{R, Kdim, N, KS, accumulate ? 1 : 0, g.wstages, g.xstages, tail, tail_col,
-               N - tail_col};
+               N - tail_col, L2Prefetch{{nullptr, nullptr, nullptr}, {0, 0, 0}}};
+  if (prefetch)
+    for (int r = 0; r < 3; ++r)
+      if (prefetch->ptr[r] && (reinterpret_cast<uintptr_t>(prefetch->ptr[r]) & 15) == 0) {
+        sh.pf.ptr[r] = prefetch->ptr[r];
+        sh.pf.bytes[r] = prefetch->bytes[r];
+      }
   const int cols = kTileN * g.mtiles;
   dim3 grid((N + cols - 1) / cols, KS, (R + 127) / 128);
   return launch(kernel, grid, dim3(128), g.smem, stream, pdl, tmW, tmX, Ypart, sh, err);

@@ -22,9 +22,19 @@ namespace kda {
 // zeros; tail_col a multiple of 128), the columns n >= tail_col are summed
 // over the splits into tail[r][n - tail_col] with fp32 atomics instead of
 // being written to Ypart.
+// Up to three device ranges that the GEMM's CTAs bring into L2 once their
+// own MMAs are done (each CTA an equal slice): data the next kernels read
+// right after the weight stream, which would otherwise be evicted by it if
+// requested earlier.
+struct L2Prefetch {
+  const void* ptr[3];
+  size_t bytes[3];
+};
+
 cudaError_t launch_tc_gemm(const kda_bf16* X2, int R, int Kdim, const kda_bf16* W, int N, int KS,
                            float* Ypart, bool accumulate, int32_t* err, cudaStream_t stream,
-                           bool pdl, float* tail = nullptr, int tail_col = 0);
+                           bool pdl, float* tail = nullptr, int tail_col = 0,
+                           const L2Prefetch* prefetch = nullptr);
 
 size_t tc_gemm_smem_bytes(int R);
 
