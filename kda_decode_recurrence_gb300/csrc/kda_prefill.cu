@@ -21,8 +21,10 @@
 // has no such bound and is served by kda_decode.
 //
 // One 256-thread CTA per (request, value head); the [128, 128] state tile is
-// held in registers in the layout of kda_decode (warp w: value columns
-// 16w .. 16w + 15; lane = (row group rg, column quad cg); rows rg + 8i).
+// held in registers in the accumulator layout of the tensor-core products
+// (warp w: value columns 16w .. 16w + 15; see the FragLane comment), and the
+// three products against it per chunk run on mma.sync with split-tf32
+// operands.
 #include <cstddef>
 
 #include "kda_async.cuh"
@@ -46,7 +48,7 @@ struct PrefillSmem {
   __align__(16) float qtT[kHeadDim][kTS];  // qh_t * exp(G_t)
   __align__(16) float kbT[kHeadDim][kTS];  // kh_t * exp(-G_t)
   __align__(16) float keT[kHeadDim][kTS];  // kh_t * exp(G_end - G_t)
-  float eGC[kHeadDim];       // exp(G_end)
+  __align__(16) float eGC[kHeadDim];  // exp(G_end)
   float A[kC][kC];           // A_ts, s < t
   float Q[kC][kC];           // Q_ts, s <= t
   __align__(16) float ws[kC][kHeadDim];  // (D_t kh_t)^T S0
@@ -173,59 +175,74 @@ __device__ __forceinline__ void stage(const DecodeArgs& p, const ChunkIn& in, bo
   if (lane == 0) sm.beta[tt] = beta;
 }
 
-// (x_t)^T S0 for tokens t0 .. t0 + 7 of a chunk, x given as xT[channel][token]:
-// in-thread partial sums over the lane's 16 rows, then a butterfly
-// reduce-scatter over the 8 row groups (lane bits 16, 8, 4).  Each lane ends
-// with one token x 4 columns fully summed and writes it to out[token][col].
-__device__ __forceinline__ void project8(const float4 (&s)[16], const float (*xT)[kTS], int t0,
-                                         float (*out)[kHeadDim], TileLane tl, int lane) {
-  float acc[8][4];
+// ---- The state on the tensor cores (mma.sync m16n8k8, tf32 inputs, fp32
+// accumulation).  Warp w owns value columns v in [16w, 16w + 16); with
+// g = lane / 4 and q = lane % 4, register sf[j][e] holds S[c][v] for
+//   c = 8j + 2q + (e & 1),  v = 16w + g + 8 (e >> 1),   j = 0..15,
+// which is the accumulator fragment of S^T (rows v, columns c) for the update
+// S^T += u^T keT^T, and -- reading positions q and q + 4 of each 8-wide
+// k block as c = 8j + 2q and 8j + 2q + 1 -- the A fragment of S^T for the
+// reads ws^T = S^T kt and qs^T = S^T qt, with no data movement.  Every fp32
+// operand is split into a tf32 part and a tf32 remainder; the three products
+// hi*hi + hi*lo + lo*hi carry about 22 significant bits (the dropped lo*lo
+// term is below 2^-22 relative).
+struct FragLane {
+  int g, q, v0;  // v0 = 16w + g
+};
+
+__device__ __forceinline__ FragLane frag_lane() {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  return FragLane{lane >> 2, lane & 3, 16 * warp + (lane >> 2)};
+}
+
+__device__ __forceinline__ void frag_tile_load(float (&sf)[16][4], const float* tile, FragLane f) {
 #pragma unroll
-  for (int t = 0; t < 8; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float* xr = xT[tl.rg + 8 * i] + t0;
-#pragma unroll
-    for (int t4 = 0; t4 < 8; t4 += 4) {
-      const float4 x4 = *reinterpret_cast<const float4*>(xr + t4);
-      const float xs[4] = {x4.x, x4.y, x4.z, x4.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int t = t4 + q;
-        acc[t][0] = fmaf(xs[q], s[i].x, acc[t][0]);
-        acc[t][1] = fmaf(xs[q], s[i].y, acc[t][1]);
-        acc[t][2] = fmaf(xs[q], s[i].z, acc[t][2]);
-        acc[t][3] = fmaf(xs[q], s[i].w, acc[t][3]);
-      }
-    }
+  for (int j = 0; j < 16; ++j) {
+    const float* r = tile + (8 * j + 2 * f.q) * kHeadDim + f.v0;
+    sf[j][0] = __ldcs(r);
+    sf[j][1] = __ldcs(r + kHeadDim);
+    sf[j][2] = __ldcs(r + 8);
+    sf[j][3] = __ldcs(r + kHeadDim + 8);
   }
-  // each round keeps the upper half of the remaining tokens where the lane
-  // bit is set and adds the partner's copy of them
-  const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4;
+}
+
+__device__ __forceinline__ void frag_tile_store(float* tile, const float (&sf)[16][4], FragLane f) {
 #pragma unroll
-  for (int t = 0; t < 4; ++t)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float send = u16 ? acc[t][j] : acc[t + 4][j];
-      const float keep = u16 ? acc[t + 4][j] : acc[t][j];
-      acc[t][j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-    }
-#pragma unroll
-  for (int t = 0; t < 2; ++t)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float send = u8 ? acc[t][j] : acc[t + 2][j];
-      const float keep = u8 ? acc[t + 2][j] : acc[t][j];
-      acc[t][j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float send = u4 ? acc[0][j] : acc[1][j];
-    const float keep = u4 ? acc[1][j] : acc[0][j];
-    acc[0][j] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  for (int j = 0; j < 16; ++j) {
+    float* r = tile + (8 * j + 2 * f.q) * kHeadDim + f.v0;
+    __stcs(r, sf[j][0]);
+    __stcs(r + kHeadDim, sf[j][1]);
+    __stcs(r + 8, sf[j][2]);
+    __stcs(r + kHeadDim + 8, sf[j][3]);
   }
-  const int t = t0 + (u16 ? 4 : 0) + (u8 ? 2 : 0) + (u4 ? 1 : 0);
-  *reinterpret_cast<float4*>(&out[t][tl.col]) = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+}
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  hi = to_tf32(x);
+  lo = to_tf32(x - __uint_as_float(hi));
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// d += (ahi + alo)(bhi + blo) without the lo * lo term, small terms first.
+__device__ __forceinline__ void mma3(float (&d)[4], const uint32_t (&ahi)[4],
+                                     const uint32_t (&alo)[4], uint32_t bh0, uint32_t bh1,
+                                     uint32_t bl0, uint32_t bl1) {
+  mma_tf32(d, alo, bh0, bh1);
+  mma_tf32(d, ahi, bl0, bl1);
+  mma_tf32(d, ahi, bh0, bh1);
 }
 
 // Two CTAs per SM (128 registers, ~100 KB of shared memory each) so that a
@@ -262,10 +279,10 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
   }
   if (t1 == t0) return;
 
-  const TileLane tl = tile_lane();
+  const FragLane fl = frag_lane();
   float* tile = p.state_pool + ((size_t)slot * p.HV + hv) * (size_t)(kHeadDim * kHeadDim);
-  float4 s[16];
-  tile_load(s, tile, tl);
+  float sf[16][4];
+  frag_tile_load(sf, tile, fl);
   const int h = hv / p.G;
   const float a_exp = expf(p.a_log[hv]);
   float* out = static_cast<float*>(p.output);
@@ -354,11 +371,46 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
           }
       }
     }
-    // ---- phase 4: (D_t kh_t)^T S0 and (D_t qh_t)^T S0 for the chunk
-    project8(s, sm.ktT, 0, sm.ws, tl, lane);
-    project8(s, sm.ktT, 8, sm.ws, tl, lane);
-    project8(s, sm.qtT, 0, sm.qs, tl, lane);
-    project8(s, sm.qtT, 8, sm.qs, tl, lane);
+    // ---- phase 4: (D_t kh_t)^T S0 and (D_t qh_t)^T S0 for the chunk, as
+    // ws^T = S0^T kt and qs^T = S0^T qt (M = the warp's 16 values, N = 16
+    // tokens in two tiles, K = the 128 channels in 16 steps of 8).
+    {
+      float aw[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      float aq[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        uint32_t ahi[4], alo[4];
+        split_tf32(sf[j][0], ahi[0], alo[0]);  // (row g,     k q)     = S[8j + 2q][v0]
+        split_tf32(sf[j][2], ahi[1], alo[1]);  // (row g + 8, k q)
+        split_tf32(sf[j][1], ahi[2], alo[2]);  // (row g,     k q + 4) = S[8j + 2q + 1][v0]
+        split_tf32(sf[j][3], ahi[3], alo[3]);  // (row g + 8, k q + 4)
+        const int c = 8 * j + 2 * fl.q;
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+          const int t = 8 * n + fl.g;  // B (k q, col g) = x[c][t], (k q + 4, col g) = x[c + 1][t]
+          uint32_t bh0, bl0, bh1, bl1;
+          split_tf32(sm.ktT[c][t], bh0, bl0);
+          split_tf32(sm.ktT[c + 1][t], bh1, bl1);
+          mma3(aw[n], ahi, alo, bh0, bh1, bl0, bl1);
+          split_tf32(sm.qtT[c][t], bh0, bl0);
+          split_tf32(sm.qtT[c + 1][t], bh1, bl1);
+          mma3(aq[n], ahi, alo, bh0, bh1, bl0, bl1);
+        }
+      }
+      // accumulator (row v, col t): (g, 2q), (g, 2q + 1), (g + 8, 2q), (g + 8, 2q + 1)
+#pragma unroll
+      for (int n = 0; n < 2; ++n) {
+        const int t = 8 * n + 2 * fl.q;
+        sm.ws[t][fl.v0] = aw[n][0];
+        sm.ws[t + 1][fl.v0] = aw[n][1];
+        sm.ws[t][fl.v0 + 8] = aw[n][2];
+        sm.ws[t + 1][fl.v0 + 8] = aw[n][3];
+        sm.qs[t][fl.v0] = aq[n][0];
+        sm.qs[t + 1][fl.v0] = aq[n][1];
+        sm.qs[t][fl.v0 + 8] = aq[n][2];
+        sm.qs[t + 1][fl.v0 + 8] = aq[n][3];
+      }
+    }
     __syncthreads();
     // ---- phase 5: the triangular solve for u, one value column per thread
     if (tid < kHeadDim) {
@@ -388,30 +440,34 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
         }
       }
     }
+    // The chunk-end state: S <- D_C S0, then S^T += u^T keT^T (M = the warp's
+    // 16 values, N = the 128 channels in 16 tiles, K = the 16 tokens in 2
+    // steps), accumulated into the state registers.
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float e = sm.eGC[tl.rg + 8 * i];
-      s[i].x *= e; s[i].y *= e; s[i].z *= e; s[i].w *= e;
+    for (int j = 0; j < 16; ++j) {
+      const float2 e = *reinterpret_cast<const float2*>(&sm.eGC[8 * j + 2 * fl.q]);
+      sf[j][0] *= e.x; sf[j][1] *= e.y; sf[j][2] *= e.x; sf[j][3] *= e.y;
     }
 #pragma unroll
-    for (int t4 = 0; t4 < kC; t4 += 4) {
-      float4 ut[4];
+    for (int kk = 0; kk < 2; ++kk) {
+      const int t = 8 * kk + fl.q;
+      uint32_t ahi[4], alo[4];
+      split_tf32(sm.u[t][fl.v0], ahi[0], alo[0]);          // (row g,     k q)
+      split_tf32(sm.u[t][fl.v0 + 8], ahi[1], alo[1]);      // (row g + 8, k q)
+      split_tf32(sm.u[t + 4][fl.v0], ahi[2], alo[2]);      // (row g,     k q + 4)
+      split_tf32(sm.u[t + 4][fl.v0 + 8], ahi[3], alo[3]);  // (row g + 8, k q + 4)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) ut[q] = *reinterpret_cast<const float4*>(&sm.u[t4 + q][tl.col]);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float4 k4 = *reinterpret_cast<const float4*>(&sm.keT[tl.rg + 8 * i][t4]);
-        const float ks[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          s[i].x = fmaf(ks[q], ut[q].x, s[i].x); s[i].y = fmaf(ks[q], ut[q].y, s[i].y);
-          s[i].z = fmaf(ks[q], ut[q].z, s[i].z); s[i].w = fmaf(ks[q], ut[q].w, s[i].w);
-        }
+      for (int j = 0; j < 16; ++j) {
+        const int c = 8 * j + fl.g;  // B (k q, col g) = keT[c][t], (k q + 4, col g) = keT[c][t + 4]
+        uint32_t bh0, bl0, bh1, bl1;
+        split_tf32(sm.keT[c][t], bh0, bl0);
+        split_tf32(sm.keT[c][t + 4], bh1, bl1);
+        mma3(sf[j], ahi, alo, bh0, bh1, bl0, bl1);
       }
     }
     __syncthreads();  // the chunk's shared arrays are consumed
   }
-  tile_store(tile, s, tl);
+  frag_tile_store(tile, sf, fl);
 }
 
 }  // namespace
