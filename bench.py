@@ -576,12 +576,14 @@ def run_profile_case(args, which: str):
     """A reduced case for ncu captures: the decode kernel on B = 32 requests x
     1 token, H = 48, HV = 96 (a 64-slot, 400 MB pool; 200 MB of state traffic
     per launch, above the L2 size), with K-first tiles ("decode") or V-first
-    tiles ("decode_vfirst", fp32 output), or the block at its full size.
+    tiles ("decode_vfirst", fp32 output), or the block at its full size with
+    n = 1 or 4 tokens per request ("block", "block_n4").
     Prints the median kernel time only."""
     from kda_decode_recurrence_gb300 import STATE_V_FIRST, kda_decode_ex
     dev = torch.device("cuda", 0)
-    if which == "block":
-        print(json.dumps({"profile": "block", **run_block(args.steps, args.warmup)}))
+    if which in ("block", "block_n4"):
+        n = 4 if which == "block_n4" else 1
+        print(json.dumps({"profile": which, **run_block(args.steps, args.warmup, n)}))
         return
     if which == "prefill":
         print(json.dumps({"profile": "prefill", **run_prefill(args.steps, args.warmup)}))
@@ -609,7 +611,8 @@ def run_profile_case(args, which: str):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile", choices=["decode", "decode_vfirst", "block", "prefill"], default=None,
+    ap.add_argument("--profile", choices=["decode", "decode_vfirst", "block", "block_n4", "prefill"],
+                    default=None,
                     help="run a reduced case of one kernel for ncu (no JSON bench line)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
