@@ -1,12 +1,16 @@
 /*
  * kda.h -- C ABI of libkda, the GB300 (sm_103a) KDA token-generation library.
  *
- * Two operations:
+ * Two operations, each with variants:
  *   kda_decode     the Kimi Delta Attention decode recurrence over a
- *                  slot-indexed fp32 state pool, varlen tokens per request.
+ *                  slot-indexed fp32 state pool, varlen tokens per request;
+ *                  kda_decode_ex chooses the state layout (K-first or V-first)
+ *                  and the output dtype (fp32 or bf16), kda_prefill computes
+ *                  the same recurrence over whole prompts in 16-token chunks.
  *   kda_block_tkg  the fused KDA block for token generation (input RMSNorm,
  *                  fused projection, short convolutions, gates, recurrence,
- *                  gated output RMSNorm, output projection).
+ *                  gated output RMSNorm, output projection), n >= 1 tokens per
+ *                  request; kda_block_tkg_static needs no caller workspace.
  *
  * Conventions shared by every call:
  *   - Every tensor pointer is a DEVICE pointer (cudaMalloc'd or equivalent),
@@ -162,7 +166,9 @@ kda_status kda_decode_ex(void* output, const kda_bf16* q, const kda_bf16* k, con
  * chunk_kda over a full sequence and fused_recurrent_kda for one new token
  * with a cache).  Arguments, layouts, outputs, state handling and device
  * status bits are those of kda_decode (K_FIRST state, fp32 output); the
- * result equals the token-by-token recurrence up to fp32 rounding.  Meant for
+ * result equals the token-by-token recurrence up to rounding (the products
+ * against the state use split-tf32 tensor-core arithmetic, about as accurate
+ * as fp32).  Meant for
  * long prompts: each request's tokens are processed 16 at a time by one CTA
  * per (request, value head).
  *
