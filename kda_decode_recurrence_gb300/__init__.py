@@ -1,15 +1,19 @@
 """GB300-native KDA token-generation library: Python binding of libkda.
 
-The two operations are the C-ABI calls of include/kda.h; this module only
-checks tensors and marshals their device pointers, sizes and the current CUDA
-stream.  Every step of the computation runs in libkda's CUDA kernels; there is
-no CPU or PyTorch fallback, and a missing library raises.
+The functions are the C-ABI calls of include/kda.h, under the same names;
+this module only checks tensors and marshals their device pointers, sizes and
+the current CUDA stream.  Every step of the computation runs in libkda's CUDA
+kernels; there is no CPU or PyTorch fallback, and a missing library raises.
 
     kda_decode(output, q, k, v, raw_gate, beta_logits, a_log, dt_bias,
                cu_seqlens, state_pool, state_indices, gate_mode, lower_bound)
+    kda_decode_ex(..., state_layout=STATE_K_FIRST | STATE_V_FIRST)
+               (the output dtype, fp32 or bf16, is taken from `output`)
+    kda_prefill(<the arguments of kda_decode>)   16-token chunks
     kda_block_tkg(out, hidden, gamma_in, W_in, W_fb, W_gb, conv_w, A_log,
                   dt_bias, gamma_o, W_o, S, conv_state, scale, lower_bound,
                   rms_norm_eps, l2_eps, workspace)
+    block_workspace_size(B, n, Hd, nh, K, V, Kc)
 """
 from __future__ import annotations
 
