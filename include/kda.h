@@ -172,10 +172,12 @@ kda_status kda_decode_ex(void* output, const kda_bf16* q, const kda_bf16* k, con
  * long prompts: each request's tokens are processed 16 at a time by one CTA
  * per (request, value head).
  *
- * Requires gate_mode == KDA_GATE_LOWER_BOUND with -5 <= lower_bound <= 0
- * ("KDA Block TKG Kernel API Reference", :param lower_bound:, the bound on
- * the cumulative decay that the chunkwise prefill depends on); otherwise it
- * returns KDA_ERR_UNSUPPORTED (use kda_decode).
+ * The chunk form needs gate_mode == KDA_GATE_LOWER_BOUND with
+ * -5 <= lower_bound <= 0 ("KDA Block TKG Kernel API Reference", :param
+ * lower_bound:, the bound on the cumulative decay that the chunkwise prefill
+ * depends on).  With the softplus gate or a lower bound below -5 the call runs
+ * kda_decode's token-by-token kernel instead: same arguments, same results as
+ * kda_decode bit for bit.
  */
 kda_status kda_prefill(float* output, const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
                        const float* raw_gate, const float* beta_logits, const float* a_log,

@@ -100,8 +100,8 @@ def kda_prefill(output, q, k, v, raw_gate, beta_logits, a_log, dt_bias, cu_seqle
                 state_indices, gate_mode=GATE_LOWER_BOUND, lower_bound=-5.0, dev_status=None,
                 stream=None, check=True) -> int:
     """Whole-prompt prefill: the kda_decode recurrence computed 16 tokens at a
-    time (lower-bound gate with lower_bound >= -5 only).  Same tensors as
-    kda_decode."""
+    time for the lower-bound gate with lower_bound >= -5; other gates run the
+    token-by-token kernel.  Same tensors as kda_decode."""
     dev = state_pool.device
     T = q.shape[-3]
     H, K = q.shape[-2], q.shape[-1]

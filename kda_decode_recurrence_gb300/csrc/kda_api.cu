@@ -123,12 +123,17 @@ kda_status kda_prefill(float* output, const kda_bf16* q, const kda_bf16* k, cons
                        const int32_t* state_indices, int gate_mode, float lower_bound, int B,
                        int T, int H, int HV, int K, int V, int max_slots, int32_t* dev_status,
                        void* stream) {
-  if (gate_mode == KDA_GATE_SOFTPLUS) return KDA_ERR_UNSUPPORTED;  // unbounded decay
-  if (gate_mode == KDA_GATE_LOWER_BOUND && std::isfinite(lower_bound) && lower_bound < -5.0f)
-    return KDA_ERR_UNSUPPORTED;
+  // The chunk form needs the decay accumulated over a chunk bounded: the
+  // lower-bound gate with lower_bound >= -5 keeps |G| <= 80, so every
+  // e^(+-G) factor is a normal fp32 number.  The softplus gate (unbounded
+  // decay) and lower bounds below -5 run the token-by-token kernel instead,
+  // which computes the same recurrence.
+  const bool chunked = !(gate_mode == KDA_GATE_SOFTPLUS ||
+                         (gate_mode == KDA_GATE_LOWER_BOUND && std::isfinite(lower_bound) &&
+                          lower_bound < -5.0f));
   return decode_impl(output, q, k, v, raw_gate, beta_logits, a_log, dt_bias, cu_seqlens,
                      state_pool, state_indices, gate_mode, lower_bound, KDA_STATE_K_FIRST,
-                     KDA_OUTPUT_F32, B, T, H, HV, K, V, max_slots, dev_status, stream, true);
+                     KDA_OUTPUT_F32, B, T, H, HV, K, V, max_slots, dev_status, stream, chunked);
 }
 
 size_t kda_block_tkg_workspace_size(int B, int n, int Hd, int nh, int K, int V, int Kc) {

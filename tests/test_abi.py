@@ -133,8 +133,11 @@ def test_decode_ex_host_validation(lib, kw, expect):
 
 
 @pytest.mark.parametrize("kw,expect", [
-    ({"gate_mode": 0}, ERR_UNSUP),                      # softplus decay is unbounded
-    ({"gate_mode": 1, "lower_bound": -6.0}, ERR_UNSUP),  # |G| over a chunk would exceed 80
+    # gates the chunk form cannot take run the token-by-token kernel: their
+    # calls validate like kda_decode's (here with no work to launch)
+    ({"gate_mode": 0, "B": 0}, KDA_OK),
+    ({"gate_mode": 1, "lower_bound": -6.0, "B": 0}, KDA_OK),
+    ({"gate_mode": 2}, ERR_ENUM),
     ({"gate_mode": 1, "lower_bound": 0.5}, ERR_VALUE),
     ({"gate_mode": 1, "K": 64}, ERR_UNSUP),
     ({"gate_mode": 1, "B": 0}, KDA_OK),

@@ -110,3 +110,17 @@ def test_q_k_v_at_an_8_byte_offset():
     assert torch.equal(out, out_a)
     slots = inp["state_indices"].long().cuda()
     assert torch.equal(d["state_pool"][slots], pool_a[slots])
+
+
+@pytest.mark.parametrize("gate,lb", [(0, -5.0), (1, -6.0)])
+def test_gates_outside_the_chunk_form_run_the_token_kernel(gate, lb):
+    # the softplus gate (unbounded decay) and lower bounds below -5 cannot use
+    # the chunk form: kda_prefill then runs the token-by-token kernel, so its
+    # results are kda_decode's bit for bit, and the oracle's within the bounds
+    inp = decode_inputs("varlen", B=4, H=2, HV=4, max_slots=6, lengths=(40, 1, 17, 33), seed=125)
+    inp["gate_mode"], inp["lower_bound"] = gate, lb
+    out_p, pool_p, st_p = gpu_prefill(inp)
+    out_d, pool_d, st_d = gpu_prefill(inp, fn=kda_decode)
+    assert st_p == 0 and st_d == 0
+    assert torch.equal(out_p, out_d) and torch.equal(pool_p, pool_d)
+    check(inp)
