@@ -373,6 +373,44 @@ def run_decode_variant(inp: dict, d: dict, steps: int) -> dict:
             "peak_source": src, "state_updates_per_s": T * HV / t}
 
 
+def run_decode_varlen(steps: int) -> dict:
+    """kda_decode on the varlen workload (64 requests of 1..8 tokens, H = HV =
+    96, lower-bound gate): the kernel's multi-token path, where each state
+    tile carries several tokens.  CUDA events per launch; the 805 MB pool is
+    far above L2."""
+    from kda_decode_recurrence_gb300 import kda_decode
+    inp = decode_inputs(DECODE_CONFIGS["varlen"])
+    dev = torch.device("cuda", torch.cuda.current_device())
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    T, H, HV, K, V, B = inp["T"], inp["H"], inp["HV"], inp["K"], inp["V"], inp["B"]
+    out = torch.empty(T, HV, V, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        kda_decode(out, d["q"], d["k"], d["v"], d["raw_gate"], d["beta_logits"], d["a_log"],
+                   d["dt_bias"], d["cu_seqlens"], d["state_pool"], d["state_indices"],
+                   gate_mode=inp["gate_mode"], lower_bound=inp["lower_bound"], stream=stream)
+
+    for _ in range(3):
+        call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for s_, e_ in ev:
+        s_.record(stream)
+        call()
+        e_.record(stream)
+    torch.cuda.synchronize(dev)
+    t = sum(s_.elapsed_time(e_) for s_, e_ in ev) * 1e-3 / steps
+    nbytes = decode_bytes(B, T, H, HV, K, V)
+    peak, src = measured_peaks()
+    return {"workload": f"varlen decode: B={B} requests of 1..8 tokens (T={T}), H=HV={HV}, "
+                        f"dk=dv={K}, pool [{inp['state_pool'].shape[0]}, {HV}, {K}, {V}] fp32, "
+                        "lower-bound gate -5",
+            "us_per_launch": t * 1e6, "launches": steps, "algorithmic_bytes": nbytes,
+            "achieved_gbs": nbytes / t / 1e9, "frac_of_hbm_peak": nbytes / t / 1e9 / peak,
+            "peak_source": src, "state_updates_per_s": T * HV / t}
+
+
 def prefill_flops(T: int, HV: int, K: int, V: int) -> int:
     """fp32 flops of the recurrence over T tokens of HV heads: per token and
     head the decay (K*V), k^T S (2 K V), the rank-1 write (2 K V) and the read
@@ -529,6 +567,7 @@ def run_gpu(args, rank, world, local):
     block = run_block(steps=max(5, min(args.steps, 50)), warmup=3) if rank == 0 else None
     block_n4 = run_block(steps=max(5, min(args.steps, 50)), warmup=3, n=4) if rank == 0 else None
     variant = run_decode_variant(inp, d, steps=max(5, min(args.steps, 200))) if rank == 0 else None
+    varlen = run_decode_varlen(steps=max(5, min(args.steps, 200))) if rank == 0 else None
     prefill = run_prefill(steps=3, warmup=1) if rank == 0 else None
 
     if rank != 0:
@@ -567,6 +606,7 @@ def run_gpu(args, rank, world, local):
         "block_tkg": block,
         "block_tkg_n4": block_n4,
         "decode_v_first_bf16": variant,
+        "decode_varlen": varlen,
         "prefill": prefill,
     }
     print(json.dumps(line), flush=True)
