@@ -13,4 +13,5 @@ from .oracle import (  # noqa: F401
     BAD_SEQLEN,
     GATE_SOFTPLUS,
     GATE_LOWER_BOUND,
+    OUT_GATES,
 )

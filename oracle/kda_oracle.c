@@ -38,6 +38,10 @@
 #define ORACLE_GATE_SOFTPLUS 0
 #define ORACLE_GATE_LOWER_BOUND 1
 
+/* Output-gate activations of the block (a reading, see output_gate). */
+#define ORACLE_OUT_GATE_SIGMOID 0
+#define ORACLE_OUT_GATE_SWISH 1
+
 /* ---------------------------------------------------------------- scalars */
 
 /* Logistic sigmoid 1 / (1 + e^-x).  [KD] beta_mode "logits"; [BT] :param
@@ -53,15 +57,30 @@ static double softplus(double x) { return (x > 0.0 ? x : 0.0) + log1p(exp(-fabs(
  *   lower-bound mode: g = lower_bound * sigmoid(exp(A_log) * (raw + dt_bias))
  * [KD] gate_mode; [BT] :param A_log: (exp(A_log) scales the gate
  * pre-activation), :param dt_bias: (added before the activation),
- * :param lower_bound:.  The exact placement of exp(A_log) and dt_bias is a
- * reading of words, not of a printed formula: parity unpinned for the gate
- * formula itself (its properties -- g <= 0, g in [lower_bound, 0] -- are
- * pinned). */
+ * :param lower_bound:.  The pages give these in words, not as a printed
+ * formula.  The reading: dt_bias joins the raw gate first, and exp(A_log)
+ * scales that whole pre-activation.  The test suite pins what the words fix:
+ * at raw = -dt_bias the pre-activation is 0, so the lower-bound gate is
+ * exactly lower_bound / 2 and the softplus gate exactly -exp(A_log) ln 2 for
+ * every A_log; the softplus gate's asymptote for large raw is
+ * -exp(A_log) (raw + dt_bias); the lower-bound gate's slope at that point is
+ * lower_bound exp(A_log) / 4; g <= 0 and g in [lower_bound, 0]. */
 static double gate_value(double raw, double dt_bias, double a_log, int gate_mode,
                          double lower_bound) {
   double x = raw + dt_bias;
   if (gate_mode == ORACLE_GATE_SOFTPLUS) return -exp(a_log) * softplus(x);
   return lower_bound * sigmoid(exp(a_log) * x);
+}
+
+/* Activation of the block's output gate z.  [BT] Background: the recurrence
+ * read goes through a "gated" output RMSNorm; the page names no activation
+ * for the gate.  Reading: the logistic sigmoid (the same squashing the page
+ * uses for the forget gate), with z * sigmoid(z) (swish) as the documented
+ * alternative.  Pinned per setting by closed forms at z = 0 and z >> 0 in
+ * the test suite; which of the two the page means is parity unpinned. */
+static double output_gate(double z, int out_gate) {
+  if (out_gate == ORACLE_OUT_GATE_SWISH) return z * sigmoid(z);
+  return sigmoid(z);
 }
 
 /* x / sqrt(sum x^2 + eps) over n entries, times mul.  [DR] Code
@@ -216,23 +235,26 @@ typedef struct {
  *   6. delta-rule recurrence on S[b, h] ([B, nh, K, V], K_FIRST), in place;
  *   7. gated output RMSNorm over V per head: z[d*nh + h] = g_a . W_gb[:, d*nh + h]
  *      (W_gb channel-outer); on = o * (mean_d o^2 + rms_norm_eps)^-1/2 *
- *      gamma_o[d] * sigmoid(z)  (gate activation: sigmoid, a reading);
+ *      gamma_o[d] * act(z), act = sigmoid (out_gate ORACLE_OUT_GATE_SIGMOID,
+ *      the default) or swish (ORACLE_OUT_GATE_SWISH): see output_gate;
  *   8. out[b, j, :] = sum_{h, d} on[h, d] * W_o[h*V + d, :]  (W_o rows taken
  *      head-outer, a reading of "dv * num_head on the partition axis").
  * Tokens j = 0 .. n-1 of a request are processed in order, the conv window and
  * S carried from one to the next.  No activation sits between f_a and W_fb.
  *
- * Parity: stages 1, 2, 3, 5, 6, 8 pinned by closed forms and layout probes in
- * the test suite; the forget-gate formula and the output-gate activation are
- * readings (parity unpinned for those two formulas). */
+ * Parity: every stage pinned by closed forms and layout probes in the test
+ * suite (the forget gate by the same closed forms as gate_value, the output
+ * gate per setting by its values at z = 0 and z >> 0).  Which output-gate
+ * activation the page means stays a reading. */
 int oracle_kda_block_tkg(double* out, const double* hidden, const double* gamma_in,
                          const double* W_in, const double* W_fb, const double* W_gb,
                          const double* conv_w, const double* A_log, const double* dt_bias,
                          const double* gamma_o, const double* W_o, double* S,
                          double* conv_state, double scale, double lower_bound,
                          double rms_norm_eps, double l2_eps, int B, int n, int Hd, int nh,
-                         int K, int V, int Kc, oracle_block_trace* tr) {
+                         int K, int V, int Kc, int out_gate, oracle_block_trace* tr) {
   if (B < 0 || n < 1 || Kc < 1) return -1;
+  if (out_gate != ORACLE_OUT_GATE_SIGMOID && out_gate != ORACLE_OUT_GATE_SWISH) return -1;
   const int CQ = K * nh, CV = V * nh;
   const int I = CQ + CQ + CV + K + nh + K;
   const int off_q = 0, off_k = CQ, off_v = 2 * CQ, off_ga = 2 * CQ + CV;
@@ -321,7 +343,7 @@ int oracle_kda_block_tkg(double* out, const double* hidden, const double* gamma_
         for (int d = 0; d < V; ++d) {
           double zz = zall[(size_t)d * nh + h]; /* W_gb columns are channel-outer */
           if (tr && tr->z) tr->z[(r * nh + h) * V + d] = zz;
-          on[(size_t)h * V + d] = o[d] * oinv * gamma_o[d] * sigmoid(zz);
+          on[(size_t)h * V + d] = o[d] * oinv * gamma_o[d] * output_gate(zz, out_gate);
         }
         if (tr) {
           for (int d = 0; d < K; ++d) {

@@ -26,6 +26,7 @@ BAD_SLOT = 1
 BAD_SEQLEN = 2
 GATE_SOFTPLUS = 0
 GATE_LOWER_BOUND = 1
+OUT_GATES = {"sigmoid": 0, "swish": 1}
 
 _lock = threading.Lock()
 _lib = None
@@ -63,7 +64,7 @@ def configure(lib):
          c_double] + [c_int] * 7 + [ip])
     lib.oracle_kda_block_tkg.restype = c_int
     lib.oracle_kda_block_tkg.argtypes = (
-        [dp] * 11 + [dp, dp] + [c_double] * 4 + [c_int] * 7 + [ctypes.POINTER(_Trace)])
+        [dp] * 11 + [dp, dp] + [c_double] * 4 + [c_int] * 8 + [ctypes.POINTER(_Trace)])
     return lib
 
 
@@ -151,13 +152,14 @@ def block_widths(nh: int, K: int, V: int) -> dict:
 
 def kda_block_tkg(hidden, gamma_in, W_in, W_fb, W_gb, conv_w, A_log, dt_bias, gamma_o, W_o,
                   S, conv_state, scale, lower_bound, rms_norm_eps=1e-5, l2_eps=1e-6,
-                  trace=False):
+                  trace=False, out_gate="sigmoid"):
     """Float64 fused KDA block.  Shapes: hidden [B, n, Hd]; gamma_in [1, Hd];
     W_in [Hd, I]; W_fb [K, K*nh]; W_gb [K, V*nh]; conv_w [3, Kc, K*nh];
     A_log [1, nh]; dt_bias [K, nh]; gamma_o [1, V]; W_o [V*nh, Hd];
     S [B, nh, K, V]; conv_state [B, 3, K*nh, Kc-1].
 
-    Returns ``(out [B, n, Hd], S_new, conv_state_new)`` and, with
+    ``out_gate`` is the output-gate activation, "sigmoid" (default) or
+    "swish".  Returns ``(out [B, n, Hd], S_new, conv_state_new)`` and, with
     ``trace=True``, a dict of the block's intermediates as a fourth item.
     The inputs are not modified.
     """
@@ -190,7 +192,7 @@ def kda_block_tkg(hidden, gamma_in, W_in, W_fb, W_gb, conv_w, A_log, dt_bias, ga
     rc = _load().oracle_kda_block_tkg(
         _dp(out), _dp(hidden), *[_dp(a) for a in args], _dp(S), _dp(conv_state),
         float(scale), float(lower_bound), float(rms_norm_eps), float(l2_eps),
-        B, n, Hd, nh, K, V, Kc, tr_ptr)
+        B, n, Hd, nh, K, V, Kc, OUT_GATES[out_gate], tr_ptr)
     if rc != 0:
         raise ValueError(f"oracle_kda_block_tkg rejected its arguments (rc={rc})")
     if trace:

@@ -6,6 +6,7 @@ subprocess; the suite must fail.  This is how the pins are shown to pin
 something: a dropped term, a flipped sign, a transposed operand, a wrong index
 or a wrong order each has to trip at least one of them.
 """
+import concurrent.futures as cf
 import os
 import subprocess
 import sys
@@ -46,29 +47,62 @@ MUTANTS = [
     ("fb_channel_outer", "double acc = graw[(size_t)h * K + d];", "double acc = graw[(size_t)d * nh + h];"),
     ("dt_bias_transposed", "(acc + dt_bias[(size_t)d * nh + h])", "(acc + dt_bias[(size_t)h * K + d])"),
     ("gb_head_outer", "double zz = zall[(size_t)d * nh + h];", "double zz = zall[(size_t)h * V + d];"),
-    ("output_gate_dropped", "on[(size_t)h * V + d] = o[d] * oinv * gamma_o[d] * sigmoid(zz);",
+    ("output_gate_dropped", "on[(size_t)h * V + d] = o[d] * oinv * gamma_o[d] * output_gate(zz, out_gate);",
      "on[(size_t)h * V + d] = o[d] * oinv * gamma_o[d];"),
-    ("output_norm_dropped", "on[(size_t)h * V + d] = o[d] * oinv * gamma_o[d] * sigmoid(zz);",
-     "on[(size_t)h * V + d] = o[d] * gamma_o[d] * sigmoid(zz);"),
+    ("output_norm_dropped", "on[(size_t)h * V + d] = o[d] * oinv * gamma_o[d] * output_gate(zz, out_gate);",
+     "on[(size_t)h * V + d] = o[d] * gamma_o[d] * output_gate(zz, out_gate);"),
+    # the other readings of the gate words: dt_bias added after the exp(A_log)
+    # scale, or the scale taken inside the softplus
+    ("gate_bias_after_scale_lower_bound", "return lower_bound * sigmoid(exp(a_log) * x);",
+     "return lower_bound * sigmoid(exp(a_log) * raw + dt_bias);"),
+    ("gate_bias_after_scale_softplus", "return -exp(a_log) * softplus(x);",
+     "return -softplus(exp(a_log) * raw + dt_bias);"),
+    ("gate_scale_inside_softplus", "return -exp(a_log) * softplus(x);",
+     "return -softplus(exp(a_log) * x);"),
+    ("block_gate_bias_after_scale", "sigmoid(exp(A_log[h]) * (acc + dt_bias[(size_t)d * nh + h]))",
+     "sigmoid(exp(A_log[h]) * acc + dt_bias[(size_t)d * nh + h])"),
+    # the two output-gate settings swapped for one another
+    ("output_gate_swish_as_default", "  return sigmoid(z);\n}", "  return z * sigmoid(z);\n}"),
+    ("output_gate_swish_setting_is_sigmoid", "if (out_gate == ORACLE_OUT_GATE_SWISH) return z * sigmoid(z);",
+     "if (out_gate == ORACLE_OUT_GATE_SWISH) return sigmoid(z);"),
 ]
 
 
-def _build_mutant(tmp_path, name, old, new):
+def _build_mutant(tmp_dir, name, old, new):
     src = open(SRC).read()
     assert src.count(old) == 1, f"mutation anchor for {name} not unique/absent"
-    path = tmp_path / f"{name}.c"
-    path.write_text(src.replace(old, new))
-    lib = tmp_path / f"{name}.so"
+    path = os.path.join(tmp_dir, f"{name}.c")
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    lib = os.path.join(tmp_dir, f"{name}.so")
     subprocess.run(["cc", "-O2", "-std=c99", "-ffp-contract=off", "-fPIC", "-shared",
-                    str(path), "-o", str(lib), "-lm"], check=True)
+                    path, "-o", lib, "-lm"], check=True)
     return lib
 
 
-@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_pins_reject_mutant(tmp_path, name, old, new):
-    lib = _build_mutant(tmp_path, name, old, new)
+def _run_pins(lib):
     env = dict(os.environ, KDA_ORACLE_LIB=str(lib))
-    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
-                       env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    return subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                           os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                          env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
+
+
+@pytest.fixture(scope="module")
+def mutant_results(tmp_path_factory):
+    """Every mutant built and run against the pin suite, several at a time
+    (each run is its own subprocess)."""
+    tmp = str(tmp_path_factory.mktemp("mutants"))
+
+    def one(m):
+        name, old, new = m
+        return name, _run_pins(_build_mutant(tmp, name, old, new))
+
+    workers = max(1, min(len(MUTANTS), os.cpu_count() or 1))
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        return dict(ex.map(one, MUTANTS))
+
+
+@pytest.mark.parametrize("name", [m[0] for m in MUTANTS])
+def test_pins_reject_mutant(mutant_results, name):
+    r = mutant_results[name]
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"

@@ -161,6 +161,102 @@ def test_safe_gate_never_amplifies():
     assert np.all(ratio <= 1.0) and np.all(ratio >= np.exp(-5.0) * (1 - 1e-15))
 
 
+# ------------------------- the gate readings, pinned by what the words fix
+#
+# "KDA Block TKG Kernel API Reference", :param dt_bias: (the bias is added
+# before the activation) and :param A_log: (exp(A_log) scales the gate
+# pre-activation); "KdaDecode", Default parameters (stable-softplus gate).
+# Read together: the pre-activation is exp(A_log) * (raw + dt_bias).  What
+# that fixes without restating the formula: at raw = -dt_bias the
+# pre-activation is zero for every A_log, so the lower-bound gate is
+# lower_bound * sigmoid(0) = lower_bound / 2 and the softplus gate is
+# -exp(A_log) * ln 2; for large raw the softplus gate runs along its asymptote
+# -exp(A_log) * (raw + dt_bias); at zero pre-activation the lower-bound gate's
+# slope in raw is lower_bound * exp(A_log) / 4.  The decay a gate produces is
+# read off the oracle's state with beta = 0 (pure decay): row k of the tile is
+# multiplied by exp(g_k).
+
+
+def decay_of(mode, raw, dt, a_log, lb=-5.0):
+    """Per-channel exp(g) as the oracle applies it: one token, beta = 0,
+    raw gate `raw` [K] and bias `dt` [K] on a single head."""
+    K = raw.shape[0]
+    rng = np.random.default_rng(5)
+    d = rand_decode(rng, B=1, H=1, HV=1, K=K, V=3, N=1, lengths=(1,), gate_mode=mode,
+                    lower_bound=lb)
+    d["raw_gate"] = raw.reshape(1, 1, K)
+    d["dt_bias"] = dt.reshape(1, K)
+    d["a_log"] = np.array([a_log])
+    d["beta_logits"][:] = -800.0
+    d["state_pool"] = 0.5 + rng.uniform(0.0, 1.0, (1, 1, K, 3))
+    _, pool, _ = run(d)
+    ratio = pool[0, 0] / d["state_pool"][0, 0]
+    assert np.allclose(ratio, ratio[:, :1], rtol=1e-15, atol=0)
+    return ratio[:, 0]
+
+
+@pytest.mark.parametrize("a_log", [0.0, np.log(2.5), np.log(16.0)])
+@pytest.mark.parametrize("lb", [-5.0, -1.3])
+def test_lower_bound_gate_is_half_the_bound_at_zero_preactivation(a_log, lb):
+    rng = np.random.default_rng(60)
+    dt = 0.3 * rng.standard_normal(8)
+    ratio = decay_of(GATE_LOWER_BOUND, -dt, dt, a_log, lb)
+    np.testing.assert_allclose(ratio, np.exp(lb / 2), rtol=1e-15)
+
+
+@pytest.mark.parametrize("a_log,expect", [(0.0, 0.5), (np.log(4.0), 1 / 16), (np.log(16.0), 2.0 ** -16)])
+def test_softplus_gate_is_exp_a_log_ln2_at_zero_preactivation(a_log, expect):
+    # g = -exp(A_log) ln 2, so exp(g) = 2^-exp(A_log): 1/2, 1/16, 2^-16
+    rng = np.random.default_rng(61)
+    dt = 0.3 * rng.standard_normal(8)
+    ratio = decay_of(GATE_SOFTPLUS, -dt, dt, a_log)
+    np.testing.assert_allclose(ratio, expect, rtol=1e-14)
+
+
+def test_softplus_gate_follows_its_asymptote_for_large_raw():
+    # For raw + dt_bias >= 25 the softplus is its argument to 2e-11 relative:
+    # g = -exp(A_log) (raw + dt_bias).  Slope and intercept both checked.
+    rng = np.random.default_rng(62)
+    a = 3.0
+    dt = 0.3 * rng.standard_normal(8)
+    raw1, raw2 = 25.0 + np.zeros(8) - dt, 31.0 + np.zeros(8) + rng.uniform(0, 1, 8)
+    g1 = np.log(decay_of(GATE_SOFTPLUS, raw1, dt, np.log(a)))
+    g2 = np.log(decay_of(GATE_SOFTPLUS, raw2, dt, np.log(a)))
+    np.testing.assert_allclose((g2 - g1) / (raw2 - raw1), -a, rtol=1e-10)
+    np.testing.assert_allclose(g1 + a * raw1, -a * dt, rtol=0, atol=1e-9)
+
+
+@pytest.mark.parametrize("a_log", [np.log(1.5), np.log(9.0)])
+def test_lower_bound_gate_slope_and_limits(a_log):
+    rng = np.random.default_rng(63)
+    dt = 0.3 * rng.standard_normal(8)
+    lb = -5.0
+    h = 1e-6
+    gp = np.log(decay_of(GATE_LOWER_BOUND, -dt + h, dt, a_log, lb))
+    gm = np.log(decay_of(GATE_LOWER_BOUND, -dt - h, dt, a_log, lb))
+    np.testing.assert_allclose((gp - gm) / (2 * h), lb * np.exp(a_log) / 4, rtol=1e-6)
+    big = np.log(decay_of(GATE_LOWER_BOUND, 60.0 - dt, dt, a_log, lb))
+    small = np.log(decay_of(GATE_LOWER_BOUND, -60.0 - dt, dt, a_log, lb))
+    np.testing.assert_allclose(big, lb, rtol=1e-15)
+    assert np.all(np.abs(small) < 1e-20)
+
+
+def test_block_forget_gate_bias_joins_the_latent_before_the_scale():
+    # One request, W_fb with a single non-zero row, so graw = f_a[0] * W_fb[0];
+    # dt_bias set to minus that: the pre-activation is zero and every channel
+    # of every head decays by exp(lower_bound / 2), whatever A_log is.
+    rng = np.random.default_rng(64)
+    p, w = block_small(rng, B=1, nh=3)
+    nh, K = 3, 4
+    p["W_fb"][1:] = 0.0
+    p["A_log"] = np.log(np.array([[1.7, 5.0, 14.0]]))
+    _, _, _, tr = oracle.kda_block_tkg(**p, trace=True)
+    alpha = tr["proj"][0, w["f_a"]]
+    p["dt_bias"] = -(alpha * p["W_fb"][0]).reshape(nh, K).T        # dt_bias[d, h]
+    _, _, _, tr = oracle.kda_block_tkg(**p, trace=True)
+    np.testing.assert_array_equal(tr["g"], np.full((1, nh, K), p["lower_bound"] / 2))
+
+
 # ----------------------------------------- (d) n tokens = n single calls
 
 
@@ -508,3 +604,46 @@ def test_block_multi_token_equals_sequential_single_tokens():
         o1, S, cs = oracle.kda_block_tkg(**q)
         assert np.array_equal(o1[:, 0], out[:, j])
     assert np.array_equal(S, S_new) and np.array_equal(cs, cs_new)
+
+
+# ------------------------------------------ the output gate, per setting
+#
+# "KDA Block TKG Kernel API Reference", Background: a "gated" output RMSNorm,
+# with no activation named.  Sigmoid is the default reading and swish
+# (z * sigmoid(z)) the alternative; each setting is pinned by its values at
+# z = 0 (W_gb = 0) and at z >> 0, where the norm alone is o / rms * gamma_o.
+
+
+def open_gate_block(rng, z_big):
+    p, w = block_small(rng)
+    p["rms_norm_eps"] = 0.0
+    K = 4
+    if z_big:
+        p["W_in"][:, w["g_a"]:w["g_a"] + K] = 0.0
+        p["W_in"][0, w["g_a"]] = 1e4
+        p["W_gb"][:] = 0.0
+        p["W_gb"][0, :] = 1.0
+        p["hidden"][..., 0] = np.abs(p["hidden"][..., 0]) + 1.0
+    else:
+        p["W_gb"][:] = 0.0
+    return p
+
+
+@pytest.mark.parametrize("gate,at_zero", [("sigmoid", 0.5), ("swish", 0.0)])
+def test_output_gate_at_zero(gate, at_zero):
+    p = open_gate_block(np.random.default_rng(70), z_big=False)
+    _, _, _, tr = oracle.kda_block_tkg(**p, trace=True, out_gate=gate)
+    assert np.all(tr["z"] == 0.0)
+    norm = tr["o"] / np.sqrt((tr["o"] ** 2).mean(-1, keepdims=True)) * p["gamma_o"][0]
+    np.testing.assert_allclose(tr["on"], at_zero * norm, rtol=1e-13, atol=0)
+
+
+@pytest.mark.parametrize("gate", ["sigmoid", "swish"])
+def test_output_gate_wide_open(gate):
+    p = open_gate_block(np.random.default_rng(71), z_big=True)
+    _, _, _, tr = oracle.kda_block_tkg(**p, trace=True, out_gate=gate)
+    assert np.all(tr["z"] > 40)
+    norm = tr["o"] / np.sqrt((tr["o"] ** 2).mean(-1, keepdims=True)) * p["gamma_o"][0]
+    # sigmoid(z) == 1 and z * sigmoid(z) == z to double precision here
+    expect = norm if gate == "sigmoid" else tr["z"] * norm
+    np.testing.assert_allclose(tr["on"], expect, rtol=1e-13, atol=0)
