@@ -202,34 +202,88 @@ def shard_seed(base_seed: int, rank: int) -> int:
 # ----------------------------------------------------------------- oracle
 
 
-def oracle_rate(inp: dict, n_requests: int):
-    """Time the float64 oracle on the first n_requests requests of a decode
-    workload (all value heads).  Returns (state-updates/s, seconds, updates)."""
-    import oracle
-    cu = inp["cu_seqlens"].numpy()
-    idx = inp["state_indices"].numpy()[:n_requests].astype(np.int64)
-    rows = np.arange(cu[0], cu[n_requests])
-    tok = {k: to_f64(inp[k][torch.from_numpy(rows)]) for k in ("q", "k", "v", "raw_gate",
-                                                                 "beta_logits")}
-    pool = to_f64(inp["state_pool"][torch.from_numpy(idx)])
-    a_log, dt_bias = to_f64(inp["a_log"]), to_f64(inp["dt_bias"])
-    cu_s = (cu[:n_requests + 1] - cu[0]).astype(np.int32)
-    t0 = time.perf_counter()
-    oracle.kda_decode(tok["q"], tok["k"], tok["v"], tok["raw_gate"], tok["beta_logits"], a_log,
-                      dt_bias, cu_s, pool, np.arange(n_requests), gate_mode=inp["gate_mode"],
-                      lower_bound=inp["lower_bound"])
-    dt = time.perf_counter() - t0
-    updates = len(rows) * inp["HV"]
-    return updates / dt, dt, updates
+def cpu_info() -> dict:
+    """The host CPU: model name (lscpu, else /proc/cpuinfo), logical CPUs,
+    and the cores this process may use."""
+    from oracle.parallel import host_cores
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not model:
+        try:
+            fields = {}
+            for line in open("/proc/cpuinfo"):
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip(), v.strip())
+            model = fields.get("model name") or (
+                f"implementer {fields.get('CPU implementer')} part {fields.get('CPU part')}"
+                if "CPU part" in fields else None)
+        except Exception:
+            pass
+    import platform
+    return {"cpu_model": model or platform.machine(), "nproc": os.cpu_count(),
+            "cores_usable": host_cores()}
 
 
-def cpu_baseline(inp: dict, budget_s: float = 12.0) -> dict:
-    rate1, dt1, _ = oracle_rate(inp, 2)
-    n = int(max(2, min(inp["B"], budget_s / max(dt1 / 2, 1e-6))))
-    rate, dt, upd = oracle_rate(inp, n)
-    return {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{n} of {inp['B']} requests x {inp['HV']} value heads ({upd} state updates, "
-                      f"{dt:.1f} s, float64 C oracle, single thread)"}
+def decode_oracle_arrays(inp: dict) -> tuple:
+    """A decode workload as the oracle workers read it: tokens (bf16 values
+    widened exactly to fp32), and the requests' state tiles in request order.
+    Returns (arrays, (gate_mode, lower_bound), state updates)."""
+    from oracle import parallel as P
+    idx = inp["state_indices"].long()
+    tok = {k: inp[k].float().numpy() for k in P.DECODE_TOKENS}
+    arrays = P.decode_arrays(tok, inp["a_log"].numpy(), inp["dt_bias"].numpy(),
+                             inp["cu_seqlens"].numpy(), inp["state_pool"][idx].numpy())
+    return arrays, (inp["gate_mode"], inp["lower_bound"]), inp["T"] * inp["HV"]
+
+
+def cpu_baseline(main_inp: dict) -> dict:
+    """The float64 oracle, as it stands, on this host: every workload (the
+    four decode ones and the block) in full, once on one thread and once
+    split by request over all usable cores (one spawned worker process per
+    core).  The headline value is the all-cores rate on the bench workload."""
+    from oracle import parallel as P
+    info = cpu_info()
+    cores = info["cores_usable"]
+    per = {}
+    with P.OracleWorkers(cores) as w:
+        for name in ("tiny", "single", "grouped", "varlen"):
+            inp = main_inp if name == WORKLOAD else decode_inputs(name)
+            arrays, extra, upd = decode_oracle_arrays(inp)
+            B = inp["B"]
+            del inp
+            t1 = P.time_single("decode", arrays, B, extra)
+            staged = w.stage(arrays)
+            del arrays
+            tn = min(w.run("decode", staged, B, extra) for _ in range(2))
+            per[name] = {"state_updates": upd, "single_thread": upd / t1, "all_cores": upd / tn,
+                         "seconds_single": t1, "seconds_all_cores": tn}
+        binp = block_inputs()
+        params = {k: binp[k].float().numpy() for k in P.BLOCK_WEIGHTS}
+        arrays = P.block_arrays(params, binp["hidden"].numpy(), binp["S"].numpy(),
+                                binp["conv_state"].numpy())
+        extra = (binp["scale"], binp["lower_bound"], binp["rms_norm_eps"], binp["l2_eps"])
+        upd = binp["B"] * binp["n"] * binp["nh"]
+        t1 = P.time_single("block", arrays, binp["B"], extra)
+        staged = w.stage(arrays)
+        tn = min(w.run("block", staged, binp["B"], extra) for _ in range(2))
+        per["block"] = {"state_updates": upd, "single_thread": upd / t1, "all_cores": upd / tn,
+                        "seconds_single": t1, "seconds_all_cores": tn}
+    main = per[WORKLOAD]
+    return {"value": main["all_cores"], "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": (f"whole workloads: every request of {WORKLOAD} (B={main_inp['B']}, "
+                       f"{main['state_updates']} state updates) and of tiny, single, varlen and "
+                       "block; float64 C oracle, split by request over one spawned process per "
+                       "core (best of 2 passes), and on one thread"),
+            "single_thread": {"value": main["single_thread"], "cores": 1},
+            "cpu_model": info["cpu_model"], "nproc": info["nproc"], "per_workload": per}
 
 
 def config_dict(cfg) -> dict:
@@ -242,33 +296,37 @@ def config_dict(cfg) -> dict:
 
 
 def run_reference(args, rank, world):
-    """The reference arm: the float64 oracle on the host cores."""
+    """The reference arm: the float64 oracle on the host cores.  Each step is
+    one pass over every request of the bench workload, split by request over
+    one spawned worker process per usable core."""
     if rank != 0:
         return
+    from oracle import parallel as P
     cfg = DECODE_CONFIGS[WORKLOAD]
     inp = decode_inputs(cfg)
-    _, dt2, _ = oracle_rate(inp, 2)
-    per_req = dt2 / 2
-    total = args.steps + args.warmup
-    n = int(max(1, min(cfg.B, 150.0 / max(total, 1) / max(per_req, 1e-6))))
-    for _ in range(args.warmup):
-        oracle_rate(inp, n)
-    times, upd = [], 0
-    for _ in range(args.steps):
-        _, dt, u = oracle_rate(inp, n)
-        times.append(dt)
-        upd = u
+    arrays, extra, upd = decode_oracle_arrays(inp)
+    B = inp["B"]
+    del inp
+    info = cpu_info()
+    cores = info["cores_usable"]
+    with P.OracleWorkers(cores) as w:
+        staged = w.stage(arrays)
+        del arrays
+        for _ in range(args.warmup):
+            w.run("decode", staged, B, extra)
+        times = [w.run("decode", staged, B, extra) for _ in range(args.steps)]
     elapsed = sum(times)
     value = upd * args.steps / elapsed
-    sample = (f"each step: {n} of {cfg.B} requests x {cfg.HV} value heads ({upd} state updates), "
-              "float64 C oracle, single thread")
+    sample = (f"each step: all {B} requests x {cfg.HV} value heads ({upd} state updates), "
+              f"float64 C oracle split by request over {cores} worker processes "
+              f"({info['cpu_model']}, {info['nproc']} logical CPUs)")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * elapsed / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_dict(cfg),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample, "cpu_model": info["cpu_model"]},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -290,9 +348,12 @@ def run_block(steps: int, warmup: int, n: int = 1) -> dict:
     names = ("hidden", "gamma_in", "W_in", "W_fb", "W_gb", "conv_w", "A_log", "dt_bias",
              "gamma_o", "W_o")
 
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
     def call():
         kda_block_tkg(out, *[d[k] for k in names], d["S"], d["conv_state"], inp["scale"],
-                      inp["lower_bound"], inp["rms_norm_eps"], inp["l2_eps"], workspace=ws)
+                      inp["lower_bound"], inp["rms_norm_eps"], inp["l2_eps"], workspace=ws,
+                      dev_status=status)
 
     for _ in range(warmup):
         call()
@@ -347,12 +408,13 @@ def run_decode_variant(inp: dict, d: dict, steps: int) -> dict:
     pool = d["state_pool"].transpose(-1, -2).contiguous()
     out = torch.empty(T, HV, V, dtype=torch.bfloat16, device=pool.device)
     stream = torch.cuda.current_stream(pool.device)
+    status = torch.zeros(1, dtype=torch.int32, device=pool.device)
 
     def call():
         kda_decode_ex(out, d["q"], d["k"], d["v"], d["raw_gate"], d["beta_logits"], d["a_log"],
                       d["dt_bias"], d["cu_seqlens"], pool, d["state_indices"],
                       gate_mode=inp["gate_mode"], lower_bound=inp["lower_bound"],
-                      state_layout=STATE_V_FIRST, stream=stream)
+                      state_layout=STATE_V_FIRST, dev_status=status, stream=stream)
 
     for _ in range(3):
         call()
@@ -385,11 +447,13 @@ def run_decode_varlen(steps: int) -> dict:
     T, H, HV, K, V, B = inp["T"], inp["H"], inp["HV"], inp["K"], inp["V"], inp["B"]
     out = torch.empty(T, HV, V, device=dev)
     stream = torch.cuda.current_stream(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def call():
         kda_decode(out, d["q"], d["k"], d["v"], d["raw_gate"], d["beta_logits"], d["a_log"],
                    d["dt_bias"], d["cu_seqlens"], d["state_pool"], d["state_indices"],
-                   gate_mode=inp["gate_mode"], lower_bound=inp["lower_bound"], stream=stream)
+                   gate_mode=inp["gate_mode"], lower_bound=inp["lower_bound"],
+                   dev_status=status, stream=stream)
 
     for _ in range(3):
         call()
@@ -437,11 +501,12 @@ def _prefill_once(steps: int, warmup: int, impl: str) -> dict:
     dev = torch.device("cuda", 0)
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     out = torch.empty(inp["T"], inp["HV"], inp["V"], device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def call():
         fn(out, d["q"], d["k"], d["v"], d["raw_gate"], d["beta_logits"], d["a_log"],
            d["dt_bias"], d["cu_seqlens"], d["state_pool"], d["state_indices"],
-           gate_mode=inp["gate_mode"], lower_bound=inp["lower_bound"])
+           gate_mode=inp["gate_mode"], lower_bound=inp["lower_bound"], dev_status=status)
 
     for _ in range(warmup):
         call()
@@ -470,11 +535,13 @@ def run_gpu(args, rank, world, local):
     B, T, H, HV, K, V = inp["B"], inp["T"], inp["H"], inp["HV"], inp["K"], inp["V"]
     out = torch.empty(T, HV, V, device=dev)
     stream = torch.cuda.current_stream(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def step():
         kda_decode(out, d["q"], d["k"], d["v"], d["raw_gate"], d["beta_logits"], d["a_log"],
                    d["dt_bias"], d["cu_seqlens"], d["state_pool"], d["state_indices"],
-                   gate_mode=inp["gate_mode"], lower_bound=inp["lower_bound"], stream=stream)
+                   gate_mode=inp["gate_mode"], lower_bound=inp["lower_bound"],
+                   dev_status=status, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -545,7 +612,8 @@ def run_gpu(args, rank, world, local):
             kda_decode(dev_out[b], dev_in[b]["q"], dev_in[b]["k"], dev_in[b]["v"],
                        dev_in[b]["raw_gate"], dev_in[b]["beta_logits"], d["a_log"], d["dt_bias"],
                        dev_in[b]["cu_seqlens"], d["state_pool"], dev_in[b]["state_indices"],
-                       gate_mode=inp["gate_mode"], lower_bound=inp["lower_bound"], stream=stream)
+                       gate_mode=inp["gate_mode"], lower_bound=inp["lower_bound"],
+                       dev_status=status, stream=stream)
             computed[b].record(stream)
             with torch.cuda.stream(out_stream):  # read back while the next step computes
                 out_stream.wait_event(computed[b])
@@ -631,6 +699,7 @@ def run_profile_case(args, which: str):
     inp = decode_inputs(DECODE_CONFIGS[WORKLOAD], B=32, max_slots=64)
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     out = torch.empty(inp["T"], inp["HV"], inp["V"], device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
     times = []
     for i in range(args.warmup + args.steps):
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -638,7 +707,8 @@ def run_profile_case(args, which: str):
         kda_decode_ex(out, d["q"], d["k"], d["v"], d["raw_gate"], d["beta_logits"], d["a_log"],
                       d["dt_bias"], d["cu_seqlens"], d["state_pool"], d["state_indices"],
                       gate_mode=inp["gate_mode"], lower_bound=inp["lower_bound"],
-                      state_layout=STATE_V_FIRST if which == "decode_vfirst" else 0)
+                      state_layout=STATE_V_FIRST if which == "decode_vfirst" else 0,
+                      dev_status=status)
         e.record()
         e.synchronize()
         if i >= args.warmup:

@@ -25,9 +25,13 @@
  *   - A host-detected problem returns a negative kda_status and launches
  *     nothing; no memory is touched.
  *   - A problem that only the device can see (a slot index out of range, a
- *     malformed cu_seqlens) never traps: the kernel skips the affected request
- *     and ORs a KDA_DEV_* bit into *dev_status (a device int32 the caller zeroes
- *     beforehand; may be NULL, in which case such errors are silent).
+ *     malformed cu_seqlens, an internal wait that gave up) never traps: the
+ *     kernel skips the affected work and ORs a KDA_DEV_* bit into *dev_status
+ *     (a device int32 the caller zeroes beforehand).  dev_status may be NULL,
+ *     but then those reports are lost: a call can leave the state partly
+ *     advanced (some requests skipped, or after KDA_DEV_TIMEOUT some tiles not
+ *     written back) with no sign of it.  Pass a status word wherever the
+ *     inputs are not known to be valid.
  *   - Calls that write the same state slots must not overlap in time.
  *
  * Page citations name the page title and the section it falls in:
@@ -205,6 +209,9 @@ kda_status kda_prefill(float* output, const kda_bf16* q, const kda_bf16* k, cons
  *   beta = sigmoid(P_beta[h]); q, k L2-normalised (l2_eps), q * scale
  *   S[b, h] advanced by the delta rule (as kda_decode), o = q^T S
  *   on = o * rsqrt(mean_d(o^2) + rms_norm_eps) * gamma_o * sigmoid(g_a . W_gb[:, d*nh + h])
+ *        (the page calls this RMSNorm "gated" without naming the activation:
+ *        sigmoid here; the library built with KDA_BLOCK_OUTPUT_GATE_SWISH=1,
+ *        shipped as libkda_outgate_swish.so, uses z * sigmoid(z) instead)
  *   out[b] = on (flattened h*V + d) . W_o
  *
  * Arguments:
@@ -256,7 +263,8 @@ kda_status kda_block_tkg(float* out, const float* hidden, const float* gamma_in,
  * workspace_bytes.
  *   - Sizes that need more than 16 MiB of workspace (see
  *     kda_block_tkg_workspace_size) return KDA_ERR_WORKSPACE before any CUDA
- *     call.
+ *     call.  Invalid sizes and B = 0 return what kda_block_tkg returns for
+ *     them, also without a CUDA call.
  *   - The first call made with a given device current looks up the array's
  *     device address on that device (cudaGetSymbolAddress) and caches it;
  *     make that first call before any stream capture.

@@ -49,6 +49,23 @@ def lib_path() -> str:
     return _build.LIB_PATH
 
 
+_variants: dict = {}
+
+
+def load_variant(name: str) -> ctypes.CDLL:
+    """Load a variant build of the library (see build.VARIANTS), e.g.
+    "outgate_swish": the fused block with a swish output gate.  Same symbols
+    and signatures as libkda.so.  Raises RuntimeError when it is missing."""
+    with _lock:
+        if name not in _variants:
+            path = _build.VARIANTS[name][0]
+            if not os.path.exists(path):
+                raise RuntimeError(f"{os.path.basename(path)} not found at {path}: build it with "
+                                   "`python -m kda_decode_recurrence_gb300.build`")
+            _variants[name] = _declare(ctypes.CDLL(path))
+    return _variants[name]
+
+
 def load(build_if_missing: bool = False) -> ctypes.CDLL:
     """Load libkda.so.  Raises RuntimeError when it is missing (no fallback)."""
     global _lib

@@ -2,7 +2,10 @@
 
 The translation units are compiled in parallel and linked into
 ``kda_decode_recurrence_gb300/_build/libkda.so`` against the shared CUDA
-runtime (the same libcudart PyTorch loads).  Usage:
+runtime (the same libcudart PyTorch loads).  A second library,
+``libkda_outgate_swish.so``, is the same build with the fused block's output
+gate compiled as swish (z * sigmoid(z)) instead of sigmoid: only kda_block.cu
+is compiled twice.  Usage:
 
     python -m kda_decode_recurrence_gb300.build [--force]
 """
@@ -20,6 +23,11 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libkda.so")
+# Library variants: name -> (library path, extra nvcc flags for kda_block.cu)
+VARIANTS = {
+    "outgate_swish": (os.path.join(BUILD_DIR, "libkda_outgate_swish.so"),
+                      ["-DKDA_BLOCK_OUTPUT_GATE_SWISH=1"]),
+}
 
 SOURCES = ["kda_api.cu", "kda_decode.cu", "kda_block.cu", "kda_tc_gemm.cu", "kda_block_static.cu", "kda_prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -50,40 +58,55 @@ def _inputs() -> list[str]:
 
 
 def _up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+    libs = [LIB_PATH] + [v[0] for v in VARIANTS.values()]
+    if not all(os.path.exists(p) for p in libs):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = min(os.path.getmtime(p) for p in libs)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link libkda.so; returns its path.  Raises on failure."""
+    """Compile and link libkda.so and its variants; returns libkda.so's path.
+    Raises on failure."""
     if not force and _up_to_date():
         return LIB_PATH
     os.makedirs(BUILD_DIR, exist_ok=True)
     nvcc = _nvcc()
 
-    def compile_one(src: str):
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-I", INCLUDE, "-I", CSRC, "-c",
+    def compile_one(job):
+        src, tag, extra = job
+        obj = os.path.join(BUILD_DIR, src.replace(".cu", f"{tag}.o"))
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-I", INCLUDE, "-I", CSRC, "-c",
                os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
-            raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+            raise RuntimeError(f"nvcc failed on {src}{tag}:\n{r.stdout}\n{r.stderr}")
         return obj, r.stderr
 
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        results = list(ex.map(compile_one, SOURCES))
+    jobs = [(src, "", []) for src in SOURCES]
+    jobs += [("kda_block.cu", f"_{name}", flags) for name, (_, flags) in VARIANTS.items()]
+    with cf.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+        results = list(ex.map(compile_one, jobs))
     if verbose:
         for _, log in results:
             sys.stderr.write(log)
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", *[o for o, _ in results], "-o", tmp,
-           "-Xlinker", f"-rpath={_cuda_lib_dir()}"]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
+    objs = [o for o, _ in results]
+    base = objs[:len(SOURCES)]
+
+    def link(objects, path):
+        tmp = path + f".tmp{os.getpid()}"
+        cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", *objects, "-o", tmp,
+               "-Xlinker", f"-rpath={_cuda_lib_dir()}"]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, path)
+
+    link(base, LIB_PATH)
+    block_obj = os.path.join(BUILD_DIR, "kda_block.o")
+    for k, (name, (path, _)) in enumerate(VARIANTS.items()):
+        variant_obj = objs[len(SOURCES) + k]
+        link([variant_obj if o == block_obj else o for o in base], path)
     return LIB_PATH
 
 

@@ -9,12 +9,15 @@
 // Kernel chain on the caller's stream (rows r = b * n + j for token j of request
 // b, R = B * n):
 //   1. rmsnorm      x = hidden * rsqrt(mean(hidden^2) + eps) * gamma_in, written
-//                   as bf16 hi/lo halves X2 [2R, Hd] for the tensor cores; out
-//                   and the projection tail zeroed
+//                   as three bf16 parts X3 [3R, Hd] (hi, lo, lo2) for the
+//                   tensor cores; out and the projection tail zeroed
 //   2. proj GEMM    tcgen05, P_part[ks] = x[:, split ks] . W_in[split ks, :]   [KS1, R, I]
 //                   (split-K so every SM streams a slice of the 103 MB W_in;
-//                   consumers add the KS1 partial sums of q, k, v; the g_a,
-//                   beta, f_a columns are summed in place into `tail`); as
+//                   consumers add the KS1 partial sums of q, k, v from hi + lo;
+//                   the g_a, beta, f_a columns take hi + lo + lo2, i.e. fp32
+//                   activations, because the forget gate amplifies their
+//                   error up to |lower_bound| exp(A_log) / 4 times, and are
+//                   summed in place into `tail`); as
 //                   its CTAs finish they bring conv_state, W_fb and W_gb
 //                   into L2 for kernels 3 and 4
 //   3. latent       graw = f_a . W_fb, z = g_a . W_gb (CUDA cores)            [R, CQ + CV]
@@ -22,7 +25,7 @@
 //                   conv + SiLU + conv_state update of the q, k, v channels,
 //                   forget gate, beta, L2 norms -> the per-head token vectors
 //                   (the same staging record kda_decode builds) and the output
-//                   gate gamma_o * sigmoid(z)
+//                   gate gamma_o * output_gate(z)
 //   5. recurrence   one CTA per (b, h): the register-tile delta-rule step on
 //                   S[b, h] (shared with kda_decode), gated output RMSNorm ->
 //                   bf16 hi/lo on2
@@ -33,12 +36,28 @@
 // windows -- before waiting); the latent kernel is launched in plain stream
 // order so that its CTAs spread over every SM.
 // Intermediates live in the caller's workspace (a few MB: L2-resident).
+//
+// Output-gate activation (the page calls the output RMSNorm "gated" and names
+// no activation): sigmoid by default; building with
+// -DKDA_BLOCK_OUTPUT_GATE_SWISH=1 selects swish, z * sigmoid(z).
 #include "kda_recurrence.cuh"
 #include "kda_launch.h"
 #include "kda_tc_gemm.h"
 
 namespace kda {
 namespace {
+
+#ifndef KDA_BLOCK_OUTPUT_GATE_SWISH
+#define KDA_BLOCK_OUTPUT_GATE_SWISH 0
+#endif
+
+__device__ __forceinline__ float output_gate(float z) {
+#if KDA_BLOCK_OUTPUT_GATE_SWISH
+  return z * sigmoidf_(z);
+#else
+  return sigmoidf_(z);
+#endif
+}
 
 constexpr int kThreads = 256;
 constexpr int kKS1 = 3;        // contraction splits of the W_in GEMM (99 tiles x 3 = 297 CTAs: one wave at 2 per SM)
@@ -65,7 +84,7 @@ bool make_layout(int B, int n, int Hd, int nh, int K, int V, int Kc, Layout* L) 
   L->KS1 = Hd / 64 < kKS1 ? Hd / 64 : kKS1;        // splits <= 64-row contraction blocks
   L->KS2 = L->CV / 64 < kKS2 ? L->CV / 64 : kKS2;
   size_t off = 0;
-  L->x2 = off;    off = align_up(off + 2 * sizeof(kda_bf16) * (size_t)L->R * Hd);
+  L->x2 = off;    off = align_up(off + 3 * sizeof(kda_bf16) * (size_t)L->R * Hd);
   L->ppart = off; off = align_up(off + sizeof(float) * (size_t)L->KS1 * L->R * L->I);
   L->tail = off;  off = align_up(off + sizeof(float) * (size_t)L->R * L->TN);
   L->gz = off;    off = align_up(off + sizeof(float) * (size_t)L->R * (L->CQ + L->CV));
@@ -84,20 +103,28 @@ __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16* hi, __nv_bflo
   *lo = __float2bfloat16_rn(x - __bfloat162float(h));
 }
 
-// The same for four consecutive values, stored as one 8-byte word per half.
-__device__ __forceinline__ void split_bf16x4(float4 x, __nv_bfloat16* hi, __nv_bfloat16* lo) {
-  const __nv_bfloat162 h01 = __floats2bfloat162_rn(x.x, x.y);
-  const __nv_bfloat162 h23 = __floats2bfloat162_rn(x.z, x.w);
-  const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
-  const __nv_bfloat162 l01 = __floats2bfloat162_rn(x.x - f01.x, x.y - f01.y);
-  const __nv_bfloat162 l23 = __floats2bfloat162_rn(x.z - f23.x, x.w - f23.y);
-  uint2 ph, pl;
-  ph.x = *reinterpret_cast<const uint32_t*>(&h01);
-  ph.y = *reinterpret_cast<const uint32_t*>(&h23);
-  pl.x = *reinterpret_cast<const uint32_t*>(&l01);
-  pl.y = *reinterpret_cast<const uint32_t*>(&l23);
-  *reinterpret_cast<uint2*>(hi) = ph;
-  *reinterpret_cast<uint2*>(lo) = pl;
+// Four consecutive values as three bf16 parts hi + lo + lo2, each stored as
+// one 8-byte word: hi = bf16(x), lo = bf16(x - hi), lo2 = bf16(x - hi - lo).
+// Both differences are exact in fp32, so hi + lo keeps ~16 significant bits
+// of x and hi + lo + lo2 all of them (to within the last bit or two).
+__device__ __forceinline__ uint2 pack_bf16x4(float a, float b, float c, float d, float4* back) {
+  const __nv_bfloat162 p01 = __floats2bfloat162_rn(a, b);
+  const __nv_bfloat162 p23 = __floats2bfloat162_rn(c, d);
+  const float2 f01 = __bfloat1622float2(p01), f23 = __bfloat1622float2(p23);
+  *back = make_float4(f01.x, f01.y, f23.x, f23.y);
+  uint2 w;
+  w.x = *reinterpret_cast<const uint32_t*>(&p01);
+  w.y = *reinterpret_cast<const uint32_t*>(&p23);
+  return w;
+}
+
+__device__ __forceinline__ void split_bf16x4_3(float4 x, __nv_bfloat16* hi, __nv_bfloat16* lo,
+                                               __nv_bfloat16* lo2) {
+  float4 h, l, l2;
+  *reinterpret_cast<uint2*>(hi) = pack_bf16x4(x.x, x.y, x.z, x.w, &h);
+  const float4 r = make_float4(x.x - h.x, x.y - h.y, x.z - h.z, x.w - h.w);
+  *reinterpret_cast<uint2*>(lo) = pack_bf16x4(r.x, r.y, r.z, r.w, &l);
+  *reinterpret_cast<uint2*>(lo2) = pack_bf16x4(r.x - l.x, r.y - l.y, r.z - l.z, r.w - l.w, &l2);
 }
 
 __device__ __forceinline__ float block_sum(float x, float* red /* [kThreads/32] */) {
@@ -116,23 +143,23 @@ constexpr int kNormThreads = 1024;
 constexpr int kNormCache = 4;  // float4 per thread held in registers (Hd <= 16384)
 
 // 1. input RMSNorm, one CTA per row: the row is read once into registers,
-// reduced, and written as bf16 hi/lo halves.  The CTA also zeroes its row of
-// `out`, which the output projection accumulates into.
+// reduced, and written as three bf16 parts (rows r, R + r, 2R + r of X3).
+// The CTA also zeroes its row of `out`, which the output projection
+// accumulates into, and its row of the projection tail.
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_split_kernel(
     const float* __restrict__ hidden, const float* __restrict__ gamma,
-    __nv_bfloat16* __restrict__ X2, float* __restrict__ out, float* __restrict__ tail, int TN,
+    __nv_bfloat16* __restrict__ X3, float* __restrict__ out, float* __restrict__ tail, int TN,
     int R, int Hd, float eps) {
   __shared__ float red[kNormThreads / 32];
   pdl_trigger();
   const float* x = hidden + (size_t)blockIdx.x * Hd;
-  float4 xv[kNormCache], gv[kNormCache];
+  float4 xv[kNormCache];  // gamma is read again at the end (an L1 / L2 hit)
   float ss = 0.f;
 #pragma unroll
   for (int c = 0; c < kNormCache; ++c) {
     const int i = (threadIdx.x + c * kNormThreads) * 4;
     const bool in = i < Hd;
     xv[c] = in ? *reinterpret_cast<const float4*>(x + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-    gv[c] = in ? *reinterpret_cast<const float4*>(gamma + i) : make_float4(0.f, 0.f, 0.f, 0.f);
     ss += xv[c].x * xv[c].x + xv[c].y * xv[c].y + xv[c].z * xv[c].z + xv[c].w * xv[c].w;
   }
   for (int i = (threadIdx.x + kNormCache * kNormThreads) * 4; i < Hd; i += kNormThreads * 4) {
@@ -146,19 +173,20 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_split_kernel(
 #pragma unroll
   for (int w = 0; w < kNormThreads / 32; ++w) tot += red[w];
   const float inv = rsqrtf(tot / (float)Hd + eps);
-  __nv_bfloat16* hi = X2 + (size_t)blockIdx.x * Hd;
-  __nv_bfloat16* lo = X2 + ((size_t)R + blockIdx.x) * Hd;
+  __nv_bfloat16* hi = X3 + (size_t)blockIdx.x * Hd;
+  __nv_bfloat16* lo = X3 + ((size_t)R + blockIdx.x) * Hd;
+  __nv_bfloat16* lo2 = X3 + ((size_t)2 * R + blockIdx.x) * Hd;
   float* orow = out + (size_t)blockIdx.x * Hd;
   for (int i = threadIdx.x; i < TN; i += kNormThreads) tail[(size_t)blockIdx.x * TN + i] = 0.f;
   auto emit = [&](int i, float4 v, float4 g) {
-    split_bf16x4(make_float4(v.x * inv * g.x, v.y * inv * g.y, v.z * inv * g.z, v.w * inv * g.w),
-                 hi + i, lo + i);
+    split_bf16x4_3(make_float4(v.x * inv * g.x, v.y * inv * g.y, v.z * inv * g.z, v.w * inv * g.w),
+                   hi + i, lo + i, lo2 + i);
     *reinterpret_cast<float4*>(orow + i) = make_float4(0.f, 0.f, 0.f, 0.f);
   };
 #pragma unroll
   for (int c = 0; c < kNormCache; ++c) {
     const int i = (threadIdx.x + c * kNormThreads) * 4;
-    if (i < Hd) emit(i, xv[c], gv[c]);
+    if (i < Hd) emit(i, xv[c], *reinterpret_cast<const float4*>(gamma + i));
   }
   for (int i = (threadIdx.x + kNormCache * kNormThreads) * 4; i < Hd; i += kNormThreads * 4)
     emit(i, *reinterpret_cast<const float4*>(x + i), *reinterpret_cast<const float4*>(gamma + i));
@@ -288,7 +316,7 @@ struct PrepArgs {
   const float* dt_bias;
   const float* gamma_o;
   TokenStage* stage;  // [R, nh]
-  float* zgate;       // [R, nh, V]: gamma_o[d] * sigmoid(z)
+  float* zgate;       // [R, nh, V]: gamma_o[d] * output_gate(z)
   float scale, lower_bound, l2_eps;
   int R, n, I, KS1, nh, Kc, CQ, CV, TN;
 };
@@ -448,7 +476,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) block_prep_kernel(const PrepA
     const float zz = p.gz[gzrow + p.CQ + (size_t)d * p.nh + h];  // W_gb channel-outer
     p.stage[(size_t)r * p.nh + h].row[d].decay =
         expf(p.lower_bound * sigmoidf_(aexp * (graw + dtb)));
-    p.zgate[((size_t)r * p.nh + h) * kHeadDim + d] = gam * sigmoidf_(zz);
+    p.zgate[((size_t)r * p.nh + h) * kHeadDim + d] = gam * output_gate(zz);
   }
   conv_save(p, chq);
   conv_save(p, chk);
@@ -563,7 +591,7 @@ cudaError_t launch_kda_block(const BlockArgs& a, cudaStream_t stream) {
                       {(size_t)a.B * 3 * L.CQ * (a.Kc - 1) * sizeof(float),
                        (size_t)a.K * L.CQ * sizeof(kda_bf16), (size_t)a.K * L.CV * sizeof(kda_bf16)}};
   e = launch_tc_gemm(reinterpret_cast<const kda_bf16*>(x2), L.R, a.Hd, a.W_in, L.I, L.KS1, ppart,
-                     false, err, stream, true, tail, L.TC, &pf);
+                     false, err, stream, true, tail, L.TC, &pf, /*x_parts=*/3);
   if (e != cudaSuccess) return e;
   // Within the tail: g_a at 0, beta at K, f_a at K + nh.
   const int off_ga = 0;

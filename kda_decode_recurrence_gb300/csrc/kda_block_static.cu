@@ -51,10 +51,16 @@ extern "C" kda_status kda_block_tkg_static(
     const float* dt_bias, const float* gamma_o, const kda_bf16* W_o, float* S, float* conv_state,
     float scale, float lower_bound, float rms_norm_eps, float l2_eps, int B, int n, int Hd, int nh,
     int K, int V, int Kc, int32_t* dev_status, void* stream) {
-  // Sizes that need more scratch than the fixed array are refused before any
-  // CUDA call.  (Invalid sizes report 0 here and are refused by the checks of
-  // kda_block_tkg below.)
-  if (kda_block_tkg_workspace_size(B, n, Hd, nh, K, V, Kc) > kScratchBytes) return KDA_ERR_WORKSPACE;
+  // Sizes that need no workspace -- invalid ones (size 0) and B == 0 -- go
+  // straight to kda_block_tkg, whose checks answer them exactly as for a
+  // caller with a workspace and make no CUDA call.  Sizes that need more
+  // scratch than the fixed array are refused, also before any CUDA call.
+  const size_t need = kda_block_tkg_workspace_size(B, n, Hd, nh, K, V, Kc);
+  if (need == 0 || B == 0)
+    return kda_block_tkg(out, hidden, gamma_in, W_in, W_fb, W_gb, conv_w, A_log, dt_bias,
+                         gamma_o, W_o, S, conv_state, scale, lower_bound, rms_norm_eps, l2_eps, B,
+                         n, Hd, nh, K, V, Kc, nullptr, 0, dev_status, stream);
+  if (need > kScratchBytes) return KDA_ERR_WORKSPACE;
   void* scratch = nullptr;
   const kda_status st = scratch_on_current_device(&scratch);
   if (st != KDA_OK) return st;

@@ -10,7 +10,10 @@
 // activations, rows R..2R-1 the bf16 rounding of the remainder, so the sum of
 // the two products carries ~16 significant bits of the activation instead of
 // 8 (the weights are exactly bf16).  The path is bound by streaming W from
-// HBM; the doubled MMA work is free.
+// HBM; the doubled MMA work is free.  Optionally X2 has a third part, rows
+// 2R..3R-1, the bf16 rounding of what hi + lo still misses: the CTAs of the
+// tail columns (tail_col and up) then add that part's product into the lo
+// accumulator too, which carries the activation to fp32 precision there.
 //
 // Mapping (swap-AB): MMA M = 128 weight columns (A = W^T tile, MN-major in
 // shared memory), MMA N = the hi and lo copies of up to 128 tokens (B = X2
@@ -110,6 +113,8 @@ struct GemmShape {
   float* tail;     // optional: columns >= tail_col are added (fp32 atomics)
   int tail_col;    // into tail[r][n - tail_col] (row stride tail_n) instead
   int tail_n;      // of being written per split
+  int x_parts;     // 2 (hi, lo) or 3 (hi, lo, lo2: the tail CTAs use lo2)
+  int xstages_tail;  // activation ring depth of the tail CTAs when x_parts == 3
   L2Prefetch pf;   // ranges to bring into L2 after the MMAs (bytes 0: none)
 };
 
@@ -135,9 +140,11 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
   const int NM = 2 * RB;                   // MMA N
   uint32_t tmem_cols = 64;                 // a power of two >= MT accumulators of NM columns
   while (tmem_cols < (uint32_t)(MT * NM)) tmem_cols *= 2;
-  const int b_bytes = NM * 128;            // hi and lo boxes, 128 B per token row
+  // Tail CTAs (whole tiles at tail_col and up) also stream the lo2 part.
+  const bool x3 = sh.x_parts == 3 && sh.tail != nullptr && n0 >= sh.tail_col;
+  const int b_bytes = (x3 ? 3 : 2) * RB * 128;  // hi, lo (and lo2) boxes, 128 B per token row
   const int a_bytes = kABytes * MT;        // one weight stage
-  const int nW = sh.wstages, nX = sh.xstages;
+  const int nW = sh.wstages, nX = x3 ? sh.xstages_tail : sh.xstages;
   const int nkb = sh.Kdim / kBK;
   const int kb0 = (int)((long long)ks * nkb / sh.KS);
   const int kb1 = (int)((long long)(ks + 1) * nkb / sh.KS);
@@ -150,6 +157,9 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
   uint64_t* xempty = xfull + kMaxXStages;
   uint64_t* done = xempty + kMaxXStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  // Progress of the three roles (k-blocks): weights and activations
+  // requested, k-blocks whose operands the MMA issuer saw arrive.
+  int* prog = reinterpret_cast<int*>(tmem_slot + 1);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < nW; ++s) {
@@ -196,7 +206,8 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
   bool ok = true;
   if (warp == 0 && lane == 0) {
     // weight producer
-    for (int kb = kb0 + pre; kb < kb1 && ok; ++kb) {
+    int kb = kb0 + pre;
+    for (; kb < kb1; ++kb) {
       const int i = kb - kb0, s = i % nW, round = i / nW;
       if (!mbar_wait(&wempty[s], (round - 1) & 1)) { ok = false; break; }
       unsigned char* a_s = wring + s * a_bytes;
@@ -208,9 +219,11 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
                     kb * kBK);
       }
     }
+    prog[0] = kb - kb0;
   } else if (warp == 2 && lane == 0) {
     // activation producer
-    for (int kb = kb0; kb < kb1 && ok; ++kb) {
+    int kb = kb0;
+    for (; kb < kb1; ++kb) {
       const int i = kb - kb0, s = i % nX, round = i / nX;
       if (i >= nX && !mbar_wait(&xempty[s], (round - 1) & 1)) { ok = false; break; }
       unsigned char* b_s = xring + s * b_bytes;
@@ -219,12 +232,18 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
       for (int j = 0; j < RB / kBoxRows; ++j) {
         tma_load_2d(b_s + j * kBoxRows * 128, &tmX, &xfull[s], k0, r0 + j * kBoxRows);
         tma_load_2d(b_s + (RB + j * kBoxRows) * 128, &tmX, &xfull[s], k0, sh.R + r0 + j * kBoxRows);
+        if (x3)
+          tma_load_2d(b_s + (2 * RB + j * kBoxRows) * 128, &tmX, &xfull[s], k0,
+                      2 * sh.R + r0 + j * kBoxRows);
       }
     }
+    prog[1] = kb - kb0;
   } else if (warp == 1 && lane == 0) {
     // MMA issuer
     const uint32_t idesc = instr_desc_bf16(NM, kTileN);
-    for (int kb = kb0; kb < kb1 && ok; ++kb) {
+    const uint32_t idesc3 = instr_desc_bf16(RB, kTileN);  // the lo2 part alone
+    int kb = kb0;
+    for (; kb < kb1; ++kb) {
       const int i = kb - kb0, sw = i % nW, sx = i % nX;
       if (!mbar_wait(&wfull[sw], (i / nW) & 1) || !mbar_wait(&xfull[sx], (i / nX) & 1)) {
         ok = false;
@@ -243,12 +262,19 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
           // away (LBO), next 8-row group 1 KiB away (SBO); 16 rows per step.
           const uint64_t adesc = smem_desc_sw128(a_addr + mt * kABytes + j * 2048, 8192, 1024);
           mma_bf16(tmem + mt * NM, adesc, bdesc, idesc, (kb > kb0 || j > 0) ? 1u : 0u);
+          // lo2 rows follow the lo rows in the stage (2*RB*128 bytes in, a
+          // multiple of 1 KiB, so the swizzle pattern lines up); their
+          // product goes into the lo accumulator, after the MMA above.
+          if (x3)
+            mma_bf16(tmem + mt * NM + RB, adesc,
+                     smem_desc_sw128(b_addr + 2 * RB * 128 + j * 32, 16, 1024), idesc3, 1u);
         }
       }
       mma_commit(&wempty[sw]);
       mma_commit(&xempty[sx]);
     }
-    mma_commit(done);
+    prog[2] = kb - kb0;
+    mma_commit(done);  // arrives once every MMA issued above has completed
   }
   __syncwarp();
 
@@ -304,6 +330,14 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(
     }
   }
   tc_fence_before();
+  if (__syncthreads_or(!have || !ok) && threadIdx.x == 0) {
+    // A wait gave up.  Let every copy this CTA requested land before its
+    // shared memory is released (bounded again): the weight and activation
+    // stages the MMA issuer had not yet seen arrive.  (The MMAs it issued
+    // are covered by the wait on `done` above.)
+    for (int i = prog[2]; i < prog[0]; ++i) mbar_wait(&wfull[i % nW], (uint32_t)(i / nW) & 1u);
+    for (int i = prog[2]; i < prog[1]; ++i) mbar_wait(&xfull[i % nX], (uint32_t)(i / nX) & 1u);
+  }
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
@@ -330,47 +364,62 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer
 // row blocks take one CTA per SM (227 KiB) with two 128-column weight tiles
 // per activation tile, which halves the activation re-reads, and 3-4
 // activation stages.
+// With three activation parts the tail CTAs stream 3*RB*128 bytes per stage:
+// they take two stages (fewer than the others above 32 rows, so that their
+// ring fits in the same shared memory).
 struct GemmRings {
-  int wstages, xstages, mtiles;
+  int wstages, xstages, xstages_tail, mtiles;
   size_t smem;
 };
 
-static GemmRings gemm_rings(int R) {
+static GemmRings gemm_rings(int R, bool x3) {
   const int rows = R < 128 ? R : 128;
   const int RB = (rows + 31) & ~31;
   const size_t b_bytes = (size_t)2 * RB * 128;
-  const size_t extra = 1024 + (2 * kMaxWStages + 2 * kMaxXStages + 1) * 8 + 16;
+  const size_t b3_bytes = (size_t)3 * RB * 128;
+  const size_t extra = 1024 + (2 * kMaxWStages + 2 * kMaxXStages + 1) * 8 + 32;
   GemmRings g;
   g.mtiles = RB <= 32 ? 1 : 2;
   const size_t budget = RB <= 32 ? 113 * 1024 : 227 * 1024;
   g.xstages = RB <= 32 ? 2 : (RB == 128 ? 3 : kMaxXStages);
+  g.xstages_tail = x3 ? (2 * g.xstages / 3 > 2 ? 2 * g.xstages / 3 : 2) : g.xstages;
+  size_t xbytes = g.xstages * b_bytes;
+  if (x3 && g.xstages_tail * b3_bytes > xbytes) xbytes = g.xstages_tail * b3_bytes;
   const size_t a_bytes = (size_t)kABytes * g.mtiles;
-  int w = (int)((budget - extra - g.xstages * b_bytes) / a_bytes);
+  int w = (int)((budget - extra - xbytes) / a_bytes);
   if (w > kMaxWStages) w = kMaxWStages;
   g.wstages = w;
-  g.smem = extra + g.xstages * b_bytes + (size_t)w * a_bytes;
+  g.smem = extra + xbytes + (size_t)w * a_bytes;
   return g;
 }
 
-size_t tc_gemm_smem_bytes(int R) { return gemm_rings(R).smem; }
+size_t tc_gemm_smem_bytes(int R) { return gemm_rings(R, false).smem; }
 
 cudaError_t launch_tc_gemm(const kda_bf16* X2, int R, int Kdim, const kda_bf16* W, int N, int KS,
                            float* Ypart, bool accumulate, int32_t* err, cudaStream_t stream,
-                           bool pdl, float* tail, int tail_col, const L2Prefetch* prefetch) {
+                           bool pdl, float* tail, int tail_col, const L2Prefetch* prefetch,
+                           int x_parts) {
   if (R < 1 || Kdim % kBK != 0 || N % 8 != 0 || KS < 1 || KS > Kdim / kBK ||
-      (tail && (tail_col % kTileN != 0 || tail_col < 0 || tail_col >= N)))
+      (tail && (tail_col % kTileN != 0 || tail_col < 0 || tail_col >= N)) ||
+      (x_parts != 2 && x_parts != 3))
     return cudaErrorInvalidValue;
+  const bool x3 = x_parts == 3 && tail != nullptr;
+  const GemmRings g = gemm_rings(R, x3);
+  // Tail CTAs must hold whole column tiles of their own (tail_col a multiple
+  // of the CTA's column span).
+  if (x3 && tail_col % (kTileN * g.mtiles) != 0) return cudaErrorInvalidValue;
   CUtensorMap tmW, tmX;
   if (!make_map(&tmW, W, (uint64_t)N, (uint64_t)Kdim, kBK)) return cudaErrorInvalidValue;
-  if (!make_map(&tmX, X2, (uint64_t)Kdim, (uint64_t)2 * R, kBoxRows)) return cudaErrorInvalidValue;
-  const GemmRings g = gemm_rings(R);
+  if (!make_map(&tmX, X2, (uint64_t)Kdim, (uint64_t)x_parts * R, kBoxRows))
+    return cudaErrorInvalidValue;
   void (*kernel)(CUtensorMap, CUtensorMap, float*, GemmShape, int32_t*) =
       g.mtiles == 2 ? tc_gemm_kernel<2> : tc_gemm_kernel<1>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)g.smem);
   if (e != cudaSuccess) return e;
   GemmShape sh{R, Kdim, N, KS, accumulate ? 1 : 0, g.wstages, g.xstages, tail, tail_col,
-               N - tail_col, L2Prefetch{{nullptr, nullptr, nullptr}, {0, 0, 0}}};
+               N - tail_col, x_parts, g.xstages_tail,
+               L2Prefetch{{nullptr, nullptr, nullptr}, {0, 0, 0}}};
   if (prefetch)
     for (int r = 0; r < 3; ++r)
       if (prefetch->ptr[r] && (reinterpret_cast<uintptr_t>(prefetch->ptr[r]) & 15) == 0) {

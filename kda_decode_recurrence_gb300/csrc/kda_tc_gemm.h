@@ -22,6 +22,9 @@ namespace kda {
 // zeros; tail_col a multiple of 128), the columns n >= tail_col are summed
 // over the splits into tail[r][n - tail_col] with fp32 atomics instead of
 // being written to Ypart.
+// With x_parts == 3, X2 is [3R, Kdim]: a third part (rows 2R..3R-1, the bf16
+// rounding of x - hi - lo) whose product the tail CTAs add as well, which
+// brings the tail columns to fp32 activation precision.
 // Up to three device ranges that the GEMM's CTAs bring into L2 once their
 // own MMAs are done (each CTA an equal slice): data the next kernels read
 // right after the weight stream, which would otherwise be evicted by it if
@@ -34,7 +37,7 @@ struct L2Prefetch {
 cudaError_t launch_tc_gemm(const kda_bf16* X2, int R, int Kdim, const kda_bf16* W, int N, int KS,
                            float* Ypart, bool accumulate, int32_t* err, cudaStream_t stream,
                            bool pdl, float* tail = nullptr, int tail_col = 0,
-                           const L2Prefetch* prefetch = nullptr);
+                           const L2Prefetch* prefetch = nullptr, int x_parts = 2);
 
 size_t tc_gemm_smem_bytes(int R);
 

@@ -38,6 +38,14 @@ def test_library_exports_every_declared_symbol(lib):
     assert lib.kda_version().decode().startswith("kda-gb300")
 
 
+@pytest.mark.parametrize("variant", sorted(build.VARIANTS))
+def test_variant_library_exports_every_declared_symbol(lib, variant):
+    vlib = _lib.load_variant(variant)
+    for name in declared_functions():
+        assert hasattr(vlib, name), name
+    assert vlib.kda_version().decode() == lib.kda_version().decode()
+
+
 def test_status_strings(lib):
     for code in _lib.STATUS:
         s = lib.kda_status_string(code).decode()

@@ -8,21 +8,23 @@ import torch
 from kda_decode_recurrence_gb300 import DEV_BAD_SLOT, kda_decode, kda_prefill
 from kda_decode_recurrence_gb300.inputs import decode_inputs
 
-from _parity import (assert_outputs_close, assert_states_close, oracle_decode_sample,
-                     to_device)
+from _parity import (Guarded, assert_outputs_close, assert_states_close, guarded_copy,
+                     oracle_decode_sample, to_device)
 
 pytestmark = pytest.mark.gpu
 
 
 def gpu_prefill(inp, fn=kda_prefill):
     d = to_device(inp)
-    out = torch.full((inp["T"], inp["HV"], inp["V"]), float("nan"), device="cuda")
+    out = Guarded((inp["T"], inp["HV"], inp["V"]), torch.float32, fill=float("nan"))
+    pool = guarded_copy(inp["state_pool"])
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    fn(out, d["q"], d["k"], d["v"], d["raw_gate"], d["beta_logits"], d["a_log"], d["dt_bias"],
-       d["cu_seqlens"], d["state_pool"], d["state_indices"], gate_mode=inp["gate_mode"],
+    fn(out.t, d["q"], d["k"], d["v"], d["raw_gate"], d["beta_logits"], d["a_log"], d["dt_bias"],
+       d["cu_seqlens"], pool.t, d["state_indices"], gate_mode=inp["gate_mode"],
        lower_bound=inp["lower_bound"], dev_status=status)
     torch.cuda.synchronize()
-    return out, d["state_pool"], int(status.item())
+    assert out.intact() and pool.intact()
+    return out.t, pool.t, int(status.item())
 
 
 def check(inp, bs=None, state_tol=1e-5):
