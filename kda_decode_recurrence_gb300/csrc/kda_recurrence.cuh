@@ -13,6 +13,15 @@
 //   S <- diag(exp(g)) S;  u = v - kh^T S;  S <- S + beta kh u^T;  o = qh^T S.
 // The read is taken as qh^T S = qh^T (D S_old) + beta (qh . kh) u, the same
 // quantity with a single pass over the tile.
+//
+// The transposed (V-first) step's arithmetic uses the packed fp32x2
+// instructions of sm_100 and later (__fmul2_rn, __ffma2_rn, __fadd2_rn: two
+// lanes per instruction, each rounded exactly like the scalar fmul/fma/add),
+// which halves its floating-point instruction count.  The row-major step
+// keeps scalar arithmetic: there a pair would be two columns of one row, each
+// row coefficient has to be broadcast into both halves, and those moves plus
+// the extra live registers made it slower (536 against 505 us per launch on
+// the grouped workload).
 #pragma once
 
 #include "kda_common.cuh"
@@ -96,6 +105,14 @@ __device__ __forceinline__ float4 tile_token_step(float4 (&s)[16], const TokenSt
                      fmaf(bqk, u.w, c.w));
 }
 
+__device__ __forceinline__ float2 f2(float x, float y) { return make_float2(x, y); }
+__device__ __forceinline__ float2 bcast2(float x) { return make_float2(x, x); }
+
+// x += the value of x in lane (this lane ^ m), both halves.
+__device__ __forceinline__ float2 xor_add2(float2 x, int m) {
+  return __fadd2_rn(x, f2(__shfl_xor_sync(0xffffffffu, x.x, m), __shfl_xor_sync(0xffffffffu, x.y, m)));
+}
+
 // ---------------------------------------------------------------------------
 // Transposed (V-first) tiles: element (k, v) sits at v * 128 + k, so the
 // contiguous direction is k.  Warp w still owns value columns [16w, 16w + 16),
@@ -143,44 +160,55 @@ __device__ __forceinline__ void tile_t_store(float* tile, const float4 (&s)[16],
       __stcs(reinterpret_cast<float4*>(tile + tile_t_offset(tl, m, c)), s[4 * m + c]);
 }
 
-__device__ __forceinline__ void decay_dot(float4& x, float4 d, float4 kh, float4 qh, float& a,
-                                          float& c) {
-  x.x *= d.x; x.y *= d.y; x.z *= d.z; x.w *= d.w;
-  a = fmaf(kh.x, x.x, a); a = fmaf(kh.y, x.y, a); a = fmaf(kh.z, x.z, a); a = fmaf(kh.w, x.w, a);
-  c = fmaf(qh.x, x.x, c); c = fmaf(qh.y, x.y, c); c = fmaf(qh.z, x.z, c); c = fmaf(qh.w, x.w, c);
+// Decay the four rows x (one column) and add their products with kh and qh
+// into the even-row / odd-row halves of a and c.
+__device__ __forceinline__ void decay_dot(float4& x, float4 d, float4 kh, float4 qh, float2& a,
+                                          float2& c) {
+  const float2 lo = __fmul2_rn(f2(x.x, x.y), f2(d.x, d.y));
+  const float2 hi = __fmul2_rn(f2(x.z, x.w), f2(d.z, d.w));
+  x = make_float4(lo.x, lo.y, hi.x, hi.y);
+  a = __ffma2_rn(f2(kh.x, kh.y), lo, a);
+  a = __ffma2_rn(f2(kh.z, kh.w), hi, a);
+  c = __ffma2_rn(f2(qh.x, qh.y), lo, c);
+  c = __ffma2_rn(f2(qh.z, qh.w), hi, c);
 }
 
 __device__ __forceinline__ void rank1(float4& x, float4 bkh, float u) {
-  x.x = fmaf(bkh.x, u, x.x); x.y = fmaf(bkh.y, u, x.y);
-  x.z = fmaf(bkh.z, u, x.z); x.w = fmaf(bkh.w, u, x.w);
+  const float2 uu = bcast2(u);
+  const float2 lo = __ffma2_rn(f2(bkh.x, bkh.y), uu, f2(x.x, x.y));
+  const float2 hi = __ffma2_rn(f2(bkh.z, bkh.w), uu, f2(x.z, x.w));
+  x = make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 
-// One token on a transposed tile (same arithmetic as tile_token_step);
-// returns the read o for the lane's four columns (identical in the 8 lanes of
-// a column quad).
+// One token on a transposed tile (same arithmetic as tile_token_step; here a
+// pair is two consecutive rows of one column, so the row sums run in two
+// halves, even and odd rows, added at the end); returns the read o for the
+// lane's four columns (identical in the 8 lanes of a column quad).
 __device__ __forceinline__ float4 tile_t_token_step(float4 (&s)[16], const TokenStageT& ts,
                                                     TileLaneT tl) {
-  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-  float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
+  float2 a[4], c[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) a[q] = c[q] = f2(0.f, 0.f);
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
     if (m == 2) asm volatile("" ::: "memory");  // bounds the hoisting of the row loads
     const int j = tl.kq + 8 * m;
     const float4 d = ts.decay[j], kh = ts.kh[j], qh = ts.qh[j];
-    decay_dot(s[4 * m + 0], d, kh, qh, a.x, c.x);
-    decay_dot(s[4 * m + 1], d, kh, qh, a.y, c.y);
-    decay_dot(s[4 * m + 2], d, kh, qh, a.z, c.z);
-    decay_dot(s[4 * m + 3], d, kh, qh, a.w, c.w);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) decay_dot(s[4 * m + q], d, kh, qh, a[q], c[q]);
   }
+  // Fold the halves, then sum over the 8 kq lanes of each column.
+  float2 a01 = f2(a[0].x, a[1].x), a23 = f2(a[2].x, a[3].x);
+  float2 c01 = f2(c[0].x, c[1].x), c23 = f2(c[2].x, c[3].x);
+  a01 = __fadd2_rn(a01, f2(a[0].y, a[1].y)); a23 = __fadd2_rn(a23, f2(a[2].y, a[3].y));
+  c01 = __fadd2_rn(c01, f2(c[0].y, c[1].y)); c23 = __fadd2_rn(c23, f2(c[2].y, c[3].y));
 #pragma unroll
   for (int m = 1; m < 8; m <<= 1) {
-    a.x += __shfl_xor_sync(0xffffffffu, a.x, m); a.y += __shfl_xor_sync(0xffffffffu, a.y, m);
-    a.z += __shfl_xor_sync(0xffffffffu, a.z, m); a.w += __shfl_xor_sync(0xffffffffu, a.w, m);
-    c.x += __shfl_xor_sync(0xffffffffu, c.x, m); c.y += __shfl_xor_sync(0xffffffffu, c.y, m);
-    c.z += __shfl_xor_sync(0xffffffffu, c.z, m); c.w += __shfl_xor_sync(0xffffffffu, c.w, m);
+    a01 = xor_add2(a01, m); a23 = xor_add2(a23, m);
+    c01 = xor_add2(c01, m); c23 = xor_add2(c23, m);
   }
   const float4 vv = *reinterpret_cast<const float4*>(&ts.v[tl.col]);
-  const float4 u = make_float4(vv.x - a.x, vv.y - a.y, vv.z - a.z, vv.w - a.w);
+  const float4 u = make_float4(vv.x - a01.x, vv.y - a01.y, vv.z - a23.x, vv.w - a23.y);
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
     const float4 bkh = ts.bkh[tl.kq + 8 * m];
@@ -189,9 +217,9 @@ __device__ __forceinline__ float4 tile_t_token_step(float4 (&s)[16], const Token
     rank1(s[4 * m + 2], bkh, u.z);
     rank1(s[4 * m + 3], bkh, u.w);
   }
-  const float bqk = ts.bqk;
-  return make_float4(fmaf(bqk, u.x, c.x), fmaf(bqk, u.y, c.y), fmaf(bqk, u.z, c.z),
-                     fmaf(bqk, u.w, c.w));
+  const float2 bq = bcast2(ts.bqk);
+  const float2 o01 = __ffma2_rn(bq, f2(u.x, u.y), c01), o23 = __ffma2_rn(bq, f2(u.z, u.w), c23);
+  return make_float4(o01.x, o01.y, o23.x, o23.y);
 }
 
 }  // namespace kda
