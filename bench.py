@@ -42,12 +42,18 @@ UNIT = "state-updates/s"
 WORKLOAD = "grouped"
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM bytes per launch of the decode kernel from one ncu capture (see
-# profiles/), tied to the kernel sources they were taken with: when the
-# sources change the figure no longer describes the kernel and is reported
-# as null.
-NCU_TRAFFIC = {"sources_sha256": "39cc73d1d4d3d48bdb271258060f50059e6652b7c466ec632d1e0a7105f800ec",
-               "bytes_per_launch": 1637349888 + 1569355776}  # read + write, grouped workload
+# DRAM bytes per launch of the decode kernel, tied to the kernel sources they
+# were taken with (when the sources change the figure no longer describes the
+# kernel and is reported as null).  Taken by ncu on the reduced case (B = 32
+# requests, one eighth of the grouped workload: `bench.py --profile decode`)
+# and scaled to the full launch: reads x 8; writes x 8 less what is still
+# dirty in L2 when the kernel ends (the reduced case's algorithmic writes
+# minus its measured ones, 55.3 MB), which does not grow with the workload.
+NCU_REDUCED = {"read": 204660992, "write": 147578368, "algorithmic_write": 202899456, "scale": 8}
+NCU_TRAFFIC = {"sources_sha256": "d1e4029f336e5713d9d782b79ca8cdcb8fe284b479d34fe3d8fbde50a29c6cf8",
+               "bytes_per_launch": (NCU_REDUCED["read"] * NCU_REDUCED["scale"]
+                                    + NCU_REDUCED["algorithmic_write"] * NCU_REDUCED["scale"]
+                                    - (NCU_REDUCED["algorithmic_write"] - NCU_REDUCED["write"]))}
 
 
 def kernel_sources_sha() -> str:
@@ -400,6 +406,38 @@ def run_block(steps: int, warmup: int, n: int = 1) -> dict:
             "state_updates_per_s": cfg.B * n * cfg.nh / t}
 
 
+def run_block_eager(steps: int, warmup: int, n: int = 1) -> dict:
+    """The block as eager C-ABI calls only (no CUDA graph), L2 flushed before
+    each: the case for kernel-level ncu captures, which cannot replay the
+    nodes of a captured graph with programmatic-dependency edges."""
+    from kda_decode_recurrence_gb300 import block_workspace_size, kda_block_tkg
+    cfg = BLOCK_CONFIG
+    inp = block_inputs(cfg, n=n)
+    d = {k: (v.to("cuda") if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    out = torch.empty(cfg.B, n, cfg.Hd, device="cuda")
+    ws = torch.empty(block_workspace_size(cfg.B, n, cfg.Hd, cfg.nh, cfg.K, cfg.V, cfg.Kc),
+                     dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    names = ("hidden", "gamma_in", "W_in", "W_fb", "W_gb", "conv_w", "A_log", "dt_bias",
+             "gamma_o", "W_o")
+    times = []
+    for i in range(warmup + steps):
+        flush.fill_(1)
+        s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_.record()
+        kda_block_tkg(out, *[d[k] for k in names], d["S"], d["conv_state"], inp["scale"],
+                      inp["lower_bound"], inp["rms_norm_eps"], inp["l2_eps"], workspace=ws,
+                      dev_status=status)
+        e_.record()
+        e_.synchronize()
+        if i >= warmup:
+            times.append(s_.elapsed_time(e_) * 1e-3)
+    assert status.item() == 0
+    return {"workload": f"kda_block_tkg B={cfg.B} n={n}, eager calls, L2 flushed before each",
+            "us_per_call": statistics.median(times) * 1e6, "calls": steps}
+
+
 def run_decode_variant(inp: dict, d: dict, steps: int) -> dict:
     """kda_decode_ex on the same workload with the transposed (V-first) state
     and bf16 output, timed like the main step (CUDA events per launch)."""
@@ -685,13 +723,18 @@ def run_profile_case(args, which: str):
     1 token, H = 48, HV = 96 (a 64-slot, 400 MB pool; 200 MB of state traffic
     per launch, above the L2 size), with K-first tiles ("decode") or V-first
     tiles ("decode_vfirst", fp32 output), or the block at its full size with
-    n = 1 or 4 tokens per request ("block", "block_n4").
+    n = 1 or 4 tokens per request ("block", "block_n4"; "*_eager": eager calls
+    only, no CUDA graph).
     Prints the median kernel time only."""
     from kda_decode_recurrence_gb300 import STATE_V_FIRST, kda_decode_ex
     dev = torch.device("cuda", 0)
     if which in ("block", "block_n4"):
         n = 4 if which == "block_n4" else 1
         print(json.dumps({"profile": which, **run_block(args.steps, args.warmup, n)}))
+        return
+    if which in ("block_eager", "block_n4_eager"):
+        n = 4 if which == "block_n4_eager" else 1
+        print(json.dumps({"profile": which, **run_block_eager(args.steps, args.warmup, n)}))
         return
     if which == "prefill":
         print(json.dumps({"profile": "prefill", **run_prefill(args.steps, args.warmup)}))
@@ -721,7 +764,8 @@ def run_profile_case(args, which: str):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile", choices=["decode", "decode_vfirst", "block", "block_n4", "prefill"],
+    ap.add_argument("--profile", choices=["decode", "decode_vfirst", "block", "block_n4",
+                                          "block_eager", "block_n4_eager", "prefill"],
                     default=None,
                     help="run a reduced case of one kernel for ncu (no JSON bench line)")
     ap.add_argument("--gpus", type=int, default=1)

@@ -2,10 +2,17 @@
 
 The translation units are compiled in parallel and linked into
 ``kda_decode_recurrence_gb300/_build/libkda.so`` against the shared CUDA
-runtime (the same libcudart PyTorch loads).  A second library,
-``libkda_outgate_swish.so``, is the same build with the fused block's output
-gate compiled as swish (z * sigmoid(z)) instead of sigmoid: only kda_block.cu
-is compiled twice.  Usage:
+runtime (the same libcudart PyTorch loads).  Two variant libraries are
+linked from the same objects with one translation unit recompiled:
+
+  libkda_outgate_swish.so  the fused block's output gate compiled as swish
+                           (z * sigmoid(z)) instead of sigmoid
+  libkda_testhooks.so      test-only: the decode kernel's copy-wait limit and
+                           one withheld work item are settable
+                           (kda_test_set_decode_hooks), to exercise its
+                           timeout report without a fault
+
+Usage:
 
     python -m kda_decode_recurrence_gb300.build [--force]
 """
@@ -23,10 +30,12 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libkda.so")
-# Library variants: name -> (library path, extra nvcc flags for kda_block.cu)
+# Library variants: name -> (library path, {source recompiled: extra nvcc flags})
 VARIANTS = {
     "outgate_swish": (os.path.join(BUILD_DIR, "libkda_outgate_swish.so"),
-                      ["-DKDA_BLOCK_OUTPUT_GATE_SWISH=1"]),
+                      {"kda_block.cu": ["-DKDA_BLOCK_OUTPUT_GATE_SWISH=1"]}),
+    "testhooks": (os.path.join(BUILD_DIR, "libkda_testhooks.so"),
+                  {"kda_decode.cu": ["-DKDA_TEST_HOOKS=1"]}),
 }
 
 SOURCES = ["kda_api.cu", "kda_decode.cu", "kda_block.cu", "kda_tc_gemm.cu", "kda_block_static.cu", "kda_prefill.cu"]
@@ -84,7 +93,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return obj, r.stderr
 
     jobs = [(src, "", []) for src in SOURCES]
-    jobs += [("kda_block.cu", f"_{name}", flags) for name, (_, flags) in VARIANTS.items()]
+    jobs += [(src, f"_{name}", flags) for name, (_, per_src) in VARIANTS.items()
+             for src, flags in per_src.items()]
     with cf.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
         results = list(ex.map(compile_one, jobs))
     if verbose:
@@ -103,10 +113,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
         os.replace(tmp, path)
 
     link(base, LIB_PATH)
-    block_obj = os.path.join(BUILD_DIR, "kda_block.o")
-    for k, (name, (path, _)) in enumerate(VARIANTS.items()):
-        variant_obj = objs[len(SOURCES) + k]
-        link([variant_obj if o == block_obj else o for o in base], path)
+    for name, (path, per_src) in VARIANTS.items():
+        swap = {os.path.join(BUILD_DIR, src.replace(".cu", ".o")):
+                os.path.join(BUILD_DIR, src.replace(".cu", f"_{name}.o")) for src in per_src}
+        link([swap.get(o, o) for o in base], path)
     return LIB_PATH
 
 

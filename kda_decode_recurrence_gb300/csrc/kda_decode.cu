@@ -209,6 +209,9 @@ __device__ __forceinline__ float* tile_ptr(const DecodeArgs& p, const Item& d) {
 // Arrive on the ring slot for `item` and start its tile copy when it has one.
 __device__ __forceinline__ void issue_item(const DecodeArgs& p, long long item, float* dst,
                                            uint64_t* bar) {
+#if KDA_TEST_HOOKS
+  if (item == p.withhold_item) return;  // test-only: this slot's phase never completes
+#endif
   const Item d = load_item(p, item);
   const bool copy = d.has_tile();
   mbar_expect_tx(bar, copy ? kTileBytes : 0u);
@@ -292,12 +295,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
     __syncwarp();  // the warp is done with the previous item's record
     bool raw_ok = true;
     if (tile) {
-      raw_ok = mbar_wait(rawbar, rawphase & 1u);
+      raw_ok = mbar_wait(rawbar, rawphase & 1u, p.wait_ns);
       ++rawphase;
       build_stage(p, read_raw_token(rawt, lane), ts, lane);
     }
 
-    const bool arrived = mbar_wait(&bars[buf], (uint32_t)(j / kBufs) & 1u);
+    const bool arrived = mbar_wait(&bars[buf], (uint32_t)(j / kBufs) & 1u, p.wait_ns);
     float4 s[16];
     if (tile && arrived) {
       const float* src = ring + buf * kHeadDim * kHeadDim;
@@ -380,8 +383,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
     if (threadIdx.x == 0) {
       raise_status(p.dev_status, KDA_DEV_TIMEOUT);
       for (int k = j; k < j + kBufs && k < nmine; ++k)
-        mbar_wait(&bars[k % kBufs], (uint32_t)(k / kBufs) & 1u);
-      if (rawphase > 0) mbar_wait(rawbar, (rawphase - 1) & 1u);  // the last first-token fill
+        mbar_wait(&bars[k % kBufs], (uint32_t)(k / kBufs) & 1u, p.wait_ns);
+      if (rawphase > 0) mbar_wait(rawbar, (rawphase - 1) & 1u, p.wait_ns);  // the last first-token fill
     }
     __syncthreads();
   }
@@ -394,7 +397,20 @@ size_t decode_smem_bytes() {
          (kBufs + 1) * sizeof(uint64_t);
 }
 
-cudaError_t launch_kda_decode(const DecodeArgs& args, cudaStream_t stream) {
+#if KDA_TEST_HOOKS
+// Test-only build: the wait limit and the withheld item of the next launches.
+unsigned long long g_test_wait_ns = kWaitLimitNs;
+long long g_test_withhold_item = -1;
+#endif
+
+cudaError_t launch_kda_decode(const DecodeArgs& in, cudaStream_t stream) {
+  DecodeArgs args = in;
+  args.wait_ns = kWaitLimitNs;
+  args.withhold_item = -1;
+#if KDA_TEST_HOOKS
+  args.wait_ns = g_test_wait_ns;
+  args.withhold_item = g_test_withhold_item;
+#endif
   const long long items = (long long)args.B * args.HV;
   if (items == 0) return cudaSuccess;
   int dev = 0, sms = 0;
@@ -415,3 +431,13 @@ cudaError_t launch_kda_decode(const DecodeArgs& args, cudaStream_t stream) {
 }
 
 }  // namespace kda
+
+#if KDA_TEST_HOOKS
+// Exported by the test-only build (libkda_testhooks.so), not declared in
+// kda.h: set the decode kernel's wait limit and the work item (request *
+// HV + value head) whose tile copy is withheld, for the launches that follow.
+extern "C" void kda_test_set_decode_hooks(long long withhold_item, unsigned long long wait_ns) {
+  kda::g_test_withhold_item = withhold_item;
+  kda::g_test_wait_ns = wait_ns;
+}
+#endif

@@ -33,6 +33,13 @@ struct DecodeArgs {
   int v_first;    // state tiles stored [V, K] instead of [K, V]
   int out_bf16;   // output written as bf16
   int B, T, H, HV, G, max_slots;
+  // Limit of every wait of the decode kernel on a copy (ns).  A test-only
+  // build of the library can shorten it and name one work item whose tile
+  // copy is never issued (withhold_item; -1: none), to exercise the path that
+  // reports KDA_DEV_TIMEOUT; the product build always runs with the full
+  // limit and no withheld item.
+  unsigned long long wait_ns;
+  long long withhold_item;
 };
 
 cudaError_t launch_kda_decode(const DecodeArgs& args, cudaStream_t stream);
