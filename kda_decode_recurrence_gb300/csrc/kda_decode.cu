@@ -28,9 +28,19 @@
 //     (normalised q and k, exp(g), beta * k, v, beta * q.k) in a private
 //     shared-memory record while the tile is in flight; later tokens of an
 //     item are staged 8 at a time, one warp per token, between two CTA
-//     barriers;
+//     barriers.  When some request has more than one token (T > B) the
+//     multi-token instance runs: warp 0's copies then bring the next item's
+//     first 9 tokens (the first token and the first round of later ones)
+//     into the shared buffer, so that round reads shared memory instead of
+//     waiting on global loads; its refill for the item after waits until
+//     that round is staged;
 //   * the advanced tile is written back from registers with 128-bit
 //     streaming stores;
+//   * in the multi-token instance every item's descriptor (slot, token
+//     range) is read from global memory once, at kernel start, into a shared
+//     table (up to kMaxDesc items per CTA), so no step on an item's path waits
+//     on a descriptor load (the single-token instances, bound by HBM, keep
+//     their loads: the table's registers slowed them);
 //   * transposed (V-first) tiles keep the same warp-to-column split, but each
 //     lane holds runs of 4 consecutive rows of its columns (the tile is
 //     contiguous along k there), with the token record laid out by field, so
@@ -100,11 +110,10 @@ __device__ __forceinline__ void cp_async_raw(void* dst, const void* src, int byt
                  : "memory");
 }
 
-// Warp 0, lane `lane`: the copies of token t (key head h, value head hv).
-// Each lane's copies arrive on `bar` (initialised for 32 arrivals) when they
-// complete, so the other warps wait for the data, not for warp 0.
-__device__ __forceinline__ void issue_raw_token(const DecodeArgs& p, RawToken* rt, uint64_t* bar,
-                                                int t, int h, int hv, int lane) {
+// One warp, lane `lane`: the copies of token t (key head h, value head hv)
+// into rt.
+__device__ __forceinline__ void copy_raw_token(const DecodeArgs& p, RawToken* rt, int t, int h,
+                                               int hv, int lane) {
   const int r0 = lane * 4;
   cp_async_raw(&rt->q[lane], p.q + ((size_t)t * p.H + h) * kHeadDim + r0, 8);
   cp_async_raw(&rt->k[lane], p.k + ((size_t)t * p.H + h) * kHeadDim + r0, 8);
@@ -115,6 +124,11 @@ __device__ __forceinline__ void issue_raw_token(const DecodeArgs& p, RawToken* r
     cp_async_raw(&rt->beta_logit, p.beta_logits + (size_t)t * p.HV + hv, 4);
     cp_async_raw(&rt->a_log, p.a_log + hv, 4);
   }
+}
+
+// This thread's arrival on `bar`, once all of its earlier cp.async copies
+// have completed.
+__device__ __forceinline__ void arrive_after_copies(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
 }
@@ -202,17 +216,44 @@ __device__ __forceinline__ Item load_item(const DecodeArgs& p, long long item) {
   return d;
 }
 
+// Descriptors kept in shared memory per CTA (slot, t0, t1 of its items j <
+// kMaxDesc); items beyond are read from global memory.
+constexpr int kMaxDesc = 512;
+
+__device__ __forceinline__ Item make_item(const DecodeArgs& p, long long item, int3 st) {
+  Item d;
+  d.b = (int)(item / p.HV);
+  d.hv = (int)(item - (long long)d.b * p.HV);
+  d.slot = st.x;
+  d.t0 = st.y;
+  d.t1 = st.z;
+  d.range_ok = d.t0 >= 0 && d.t1 >= d.t0 && d.t1 <= p.T;
+  d.slot_ok = d.slot >= 0 && d.slot < p.max_slots;
+  return d;
+}
+
+// Item j of this CTA (global index first + j * G): from the shared table in
+// the multi-token instance, else from global memory.
+template <bool kMulti>
+__device__ __forceinline__ Item get_item(const DecodeArgs& p, const int3* desc, long long first,
+                                         long long G, int j) {
+  const long long item = first + (long long)j * G;
+  return kMulti && j < kMaxDesc ? make_item(p, item, desc[j]) : load_item(p, item);
+}
+
 __device__ __forceinline__ float* tile_ptr(const DecodeArgs& p, const Item& d) {
   return p.state_pool + ((size_t)d.slot * p.HV + d.hv) * (size_t)(kHeadDim * kHeadDim);
 }
 
-// Arrive on the ring slot for `item` and start its tile copy when it has one.
-__device__ __forceinline__ void issue_item(const DecodeArgs& p, long long item, float* dst,
-                                           uint64_t* bar) {
+// Arrive on the ring slot for item d (global index `item`) and start its
+// tile copy when it has one.
+__device__ __forceinline__ void issue_item(const DecodeArgs& p, const Item& d, long long item,
+                                           float* dst, uint64_t* bar) {
 #if KDA_TEST_HOOKS
   if (item == p.withhold_item) return;  // test-only: this slot's phase never completes
+#else
+  (void)item;
 #endif
-  const Item d = load_item(p, item);
   const bool copy = d.has_tile();
   mbar_expect_tx(bar, copy ? kTileBytes : 0u);
   if (copy) bulk_load(dst, tile_ptr(p, d), kTileBytes, bar);
@@ -243,11 +284,33 @@ __device__ __forceinline__ void store_out(const DecodeArgs& p, int t, int hv, in
   }
 }
 
+// Fill the raw buffer with item dn's first token -- and in the multi-token
+// instance with the first round of its later tokens too (up to 1 + kWarps
+// tokens).  Single-token instance: warp 0 copies the one token and its 32
+// lanes arrive on `bar`.  Multi-token instance: warp w copies token w (warp 0
+// also the last one), and all kThreads threads arrive.  Called by the threads
+// that arrive; a no-op for an item without a tile (no phase: its consumers do
+// not wait).
+template <bool kMulti>
+__device__ __forceinline__ void refill_raw(const DecodeArgs& p, RawToken* rawt, uint64_t* bar,
+                                           const Item& dn, int warp, int lane) {
+  if (!dn.has_tile()) return;
+  const int h = dn.hv / p.G;
+  if (kMulti) {
+    const int ntok = min(1 + kWarps, dn.t1 - dn.t0);
+    for (int i = warp; i < ntok; i += kWarps) copy_raw_token(p, &rawt[i], dn.t0 + i, h, dn.hv, lane);
+  } else {
+    copy_raw_token(p, rawt, dn.t0, h, dn.hv, lane);
+  }
+  arrive_after_copies(bar);
+}
+
 // kVFirst: tiles are stored [V, K] (row v contiguous over k, the layout of a
 // transposed state); the lanes then hold runs of 4 rows of one column
 // (TileLaneT, tile_t_token_step), so tile loads and stores stay 128-bit and
-// conflict-free.
-template <bool kVFirst, bool kOutBf16>
+// conflict-free.  kMulti: the multi-token instance (raw buffer of 1 + kWarps
+// tokens).
+template <bool kVFirst, bool kOutBf16, bool kMulti>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const DecodeArgs p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   float* ring = reinterpret_cast<float*>(
@@ -255,8 +318,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
   using Stage = typename std::conditional<kVFirst, TokenStageT, TokenStage>::type;
   Stage* wstage = reinterpret_cast<Stage*>(ring + kBufs * kHeadDim * kHeadDim);
   RawToken* rawt = reinterpret_cast<RawToken*>(wstage + kWarps);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(rawt + 1);
-  uint64_t* rawbar = bars + kBufs;  // the first-token copies (32 arrivals: warp 0's lanes)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(rawt + (kMulti ? 1 + kWarps : 1));
+  // The raw buffer's fills (32 arrivals, warp 0's lanes; kThreads in the
+  // multi-token instance).
+  uint64_t* rawbar = bars + kBufs;
+  int3* desc = reinterpret_cast<int3*>(rawbar + 1);  // [kMaxDesc] slot, t0, t1
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -273,22 +339,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
     raise_status(p.dev_status, KDA_DEV_BAD_SEQLEN);
   if (threadIdx.x == 0) {
     for (int i = 0; i < kBufs; ++i) mbar_init(&bars[i], 1);
-    mbar_init(rawbar, 32);
+    mbar_init(rawbar, kMulti ? kThreads : 32);
     mbar_fence_init();
     for (int j = 0; j < kBufs && j < nmine; ++j)
-      issue_item(p, first + j * G, ring + j * kHeadDim * kHeadDim, &bars[j]);
+      issue_item(p, load_item(p, first + j * G), first + j * G, ring + j * kHeadDim * kHeadDim,
+                 &bars[j]);
   }
-  __syncthreads();  // the barriers are initialised
-  if (warp == 0 && nmine > 0) {
-    const Item d0 = load_item(p, first);
-    if (d0.has_tile()) issue_raw_token(p, rawt, rawbar, d0.t0, d0.hv / p.G, d0.hv, lane);
+  if (kMulti) {
+    for (int i = threadIdx.x; i < nmine && i < kMaxDesc; i += kThreads) {
+      const int b = (int)((first + (long long)i * G) / p.HV);
+      desc[i] = make_int3(__ldg(p.state_indices + b), __ldg(p.cu_seqlens + b),
+                          __ldg(p.cu_seqlens + b + 1));
+    }
   }
+  __syncthreads();  // the barriers are initialised and the descriptors in place
+  if ((kMulti || warp == 0) && nmine > 0)
+    refill_raw<kMulti>(p, rawt, rawbar, get_item<kMulti>(p, desc, first, G, 0), warp, lane);
   uint32_t rawphase = 0;  // fills of the first-token buffer consumed so far
 
   int j = 0;
   for (; j < nmine; ++j) {
     const int buf = j % kBufs;
-    const Item d = load_item(p, first + (long long)j * G);
+    const Item d = get_item<kMulti>(p, desc, first, G, j);
     const bool tile = d.has_tile();
     const int h = d.hv / p.G;
     // The item's first-token inputs, copied by warp 0 during the previous item.
@@ -321,14 +393,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
     // buffer the next item's first token.
     if (__syncthreads_or(!arrived || !raw_ok)) break;
     if (threadIdx.x == 0 && j + kBufs < nmine)
-      issue_item(p, first + (long long)(j + kBufs) * G, ring + buf * kHeadDim * kHeadDim,
-                 &bars[buf]);
-    // Every warp has built its record from the raw buffer: warp 0 refills it
-    // with the next item's first token.
-    if (warp == 0 && j + 1 < nmine) {
-      const Item dn = load_item(p, first + (long long)(j + 1) * G);
-      if (dn.has_tile()) issue_raw_token(p, rawt, rawbar, dn.t0, dn.hv / p.G, dn.hv, lane);
-    }
+      issue_item(p, get_item<kMulti>(p, desc, first, G, j + kBufs),
+                 first + (long long)(j + kBufs) * G, ring + buf * kHeadDim * kHeadDim, &bars[buf]);
+    // Every warp has built its record from the raw buffer: it is refilled
+    // with the next item's first token(s) -- in the multi-token instance not
+    // before this item's first round has been staged from it.
+    const bool has_round = kMulti && tile && d.t1 - d.t0 > 1;
+    if ((kMulti || warp == 0) && j + 1 < nmine && !has_round)
+      refill_raw<kMulti>(p, rawt, rawbar, get_item<kMulti>(p, desc, first, G, j + 1), warp, lane);
 
     if (!d.range_ok) {
       if (d.hv == 0 && threadIdx.x == 0) raise_status(p.dev_status, KDA_DEV_BAD_SEQLEN);
@@ -357,9 +429,22 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
     // every thread handles the same item.)
     for (int c0 = d.t0 + 1; c0 < d.t1; c0 += kWarps) {
       const int nc = min(kWarps, d.t1 - c0);
-      __syncthreads();  // all warps are done with the records of the last round
-      if (warp < nc) build_stage(p, fetch_token(p, c0 + warp, h, d.hv, lane), wstage[warp], lane);
-      __syncthreads();
+      if (kMulti && c0 == d.t0 + 1) {
+        // First round: its rows came with the first token's copies.  Until
+        // now each warp has read only its own record, so it may refill it as
+        // soon as its lanes are done with it.
+        __syncwarp();
+        if (warp < nc) build_stage(p, read_raw_token(&rawt[1 + warp], lane), wstage[warp], lane);
+        __syncthreads();
+        // The raw buffer is free: refill it for the next item.
+        if (j + 1 < nmine)
+          refill_raw<kMulti>(p, rawt, rawbar, get_item<kMulti>(p, desc, first, G, j + 1), warp,
+                             lane);
+      } else {
+        __syncthreads();  // all warps are done with the records of the last round
+        if (warp < nc) build_stage(p, fetch_token(p, c0 + warp, h, d.hv, lane), wstage[warp], lane);
+        __syncthreads();
+      }
       for (int jj = 0; jj < nc; ++jj) {
         const float4 o = step(s, wstage[jj], tl, tlt);
         if (kVFirst ? tlt.kq == 0 : tl.rg == 0)
@@ -392,9 +477,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
 
 }  // namespace
 
-size_t decode_smem_bytes() {
-  return 128 + (size_t)kBufs * kTileBytes + kWarps * sizeof(TokenStage) + sizeof(RawToken) +
-         (kBufs + 1) * sizeof(uint64_t);
+size_t decode_smem_bytes(bool multi) {
+  return 128 + (size_t)kBufs * kTileBytes + kWarps * sizeof(TokenStage) +
+         (multi ? 1 + kWarps : 1) * sizeof(RawToken) + (kBufs + 1) * sizeof(uint64_t) +
+         (multi ? kMaxDesc * sizeof(int3) : 0);
 }
 
 #if KDA_TEST_HOOKS
@@ -418,10 +504,16 @@ cudaError_t launch_kda_decode(const DecodeArgs& in, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const size_t smem = decode_smem_bytes();
+  // The multi-token instance when some request has more than one token.
+  const bool multi = args.T > args.B;
+  const size_t smem = decode_smem_bytes(multi);
   void (*kernel)(DecodeArgs) =
-      args.v_first ? (args.out_bf16 ? kda_decode_kernel<true, true> : kda_decode_kernel<true, false>)
-                   : (args.out_bf16 ? kda_decode_kernel<false, true> : kda_decode_kernel<false, false>);
+      multi ? (args.v_first
+                   ? (args.out_bf16 ? kda_decode_kernel<true, true, true> : kda_decode_kernel<true, false, true>)
+                   : (args.out_bf16 ? kda_decode_kernel<false, true, true> : kda_decode_kernel<false, false, true>))
+            : (args.v_first
+                   ? (args.out_bf16 ? kda_decode_kernel<true, true, false> : kda_decode_kernel<true, false, false>)
+                   : (args.out_bf16 ? kda_decode_kernel<false, true, false> : kda_decode_kernel<false, false, false>));
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const long long slots = (long long)sms * kCtasPerSm;
