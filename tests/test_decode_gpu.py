@@ -10,6 +10,8 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
+
 from kda_decode_recurrence_gb300 import DEV_BAD_SEQLEN, DEV_BAD_SLOT, GATE_LOWER_BOUND, kda_decode
 from kda_decode_recurrence_gb300.inputs import decode_inputs, to_f64
 
@@ -340,4 +342,61 @@ def test_pool_larger_than_4_gib():
     assert_states_close(got, ref_pool)
     assert bool((pool[sentinels] == 7.0).all())
     del pool
+    torch.cuda.empty_cache()
+
+
+def test_multi_token_items_beyond_the_descriptor_table():
+    # The multi-token kernel (T > B) keeps up to 512 item descriptors per CTA
+    # in shared memory and reads any later ones from global memory.  With more
+    # than 512 items per CTA (a persistent grid of 2 CTAs per SM), every CTA
+    # crosses that boundary.  The pool then holds over 10 GB of tiles: only
+    # the sampled requests' slots get seeded values, the rest stay zero (a
+    # valid state); requests on both sides of the boundary are checked.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    grid = 2 * sms
+    H = HV = 32
+    B = (512 * grid) // HV + 40                      # 40 requests' items past the table
+    lengths = 1 + np.arange(B) % 2                   # T > B: the multi-token kernel
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    T = int(cu[-1])
+    rng = np.random.default_rng(150)
+    tok = {"q": rng.standard_normal((T, H, 128), dtype=np.float32),
+           "k": rng.standard_normal((T, H, 128), dtype=np.float32),
+           "v": rng.standard_normal((T, HV, 128), dtype=np.float32),
+           "raw_gate": rng.standard_normal((T, HV, 128), dtype=np.float32),
+           "beta_logits": rng.standard_normal((T, HV), dtype=np.float32)}
+    a_log = np.log(rng.uniform(1, 16, HV)).astype(np.float32)
+    dt_bias = (0.1 * rng.standard_normal((HV, 128))).astype(np.float32)
+    sample = list(range(8)) + list(range(B - 64, B))
+    slots = rng.permutation(B).astype(np.int32)       # request b -> slot slots[b]
+    tiles = (0.05 * rng.standard_normal((len(sample), HV, 128, 128))).astype(np.float32)
+    dev = "cuda"
+    tq = {k_: torch.from_numpy(v_) for k_, v_ in tok.items()}
+    for name in ("q", "k", "v"):
+        tq[name] = tq[name].to(torch.bfloat16)
+    d = {k_: v_.to(dev) for k_, v_ in tq.items()}
+    pool = Guarded((B, HV, 128, 128), torch.float32, dev, fill=0.0)
+    pool.t[torch.from_numpy(slots[sample].astype(np.int64)).to(dev)] = torch.from_numpy(tiles).to(dev)
+    out = Guarded((T, HV, 128), torch.float32, dev, fill=float("nan"))
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    kda_decode(out.t, d["q"], d["k"], d["v"], d["raw_gate"], d["beta_logits"],
+               torch.from_numpy(a_log).to(dev), torch.from_numpy(dt_bias).to(dev),
+               torch.from_numpy(cu).to(dev), pool.t, torch.from_numpy(slots).to(dev),
+               gate_mode=GATE_LOWER_BOUND, lower_bound=-5.0, dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0 and out.intact() and pool.intact()
+    assert torch.isfinite(out.t).all().item()
+    # the oracle on the sampled requests, with their exact (bf16-rounded) inputs
+    rows = np.concatenate([np.arange(cu[b], cu[b + 1]) for b in sample])
+    sub = {k_: to_f64(tq[k_][torch.from_numpy(rows)]) for k_ in tq}
+    ref_out, ref_pool, st = oracle.kda_decode(
+        sub["q"], sub["k"], sub["v"], sub["raw_gate"], sub["beta_logits"], a_log.astype(np.float64),
+        dt_bias.astype(np.float64), np.concatenate([[0], np.cumsum(lengths[sample])]),
+        tiles.astype(np.float64), np.arange(len(sample)), gate_mode=GATE_LOWER_BOUND,
+        lower_bound=-5.0)
+    assert st == 0
+    assert_outputs_close(out.t[torch.from_numpy(rows).to(dev)].cpu().numpy(), ref_out)
+    got = pool.t[torch.from_numpy(slots[sample].astype(np.int64)).to(dev)].cpu().numpy()
+    assert_states_close(got, ref_pool)
+    del pool, out
     torch.cuda.empty_cache()
