@@ -284,33 +284,31 @@ __device__ __forceinline__ void store_out(const DecodeArgs& p, int t, int hv, in
   }
 }
 
-// Fill the raw buffer with item dn's first token -- and in the multi-token
-// instance with the first round of its later tokens too (up to 1 + kWarps
-// tokens).  Single-token instance: warp 0 copies the one token and its 32
-// lanes arrive on `bar`.  Multi-token instance: warp w copies token w (warp 0
-// also the last one), and all kThreads threads arrive.  Called by the threads
-// that arrive; a no-op for an item without a tile (no phase: its consumers do
-// not wait).
+// Fill the raw buffer with item dn's first token -- in the multi-token
+// schedule with its whole first round (up to kWarps tokens).  Single-token
+// schedule: warp 0 copies the one token and its 32 lanes arrive on `bar`.
+// Multi-token schedule: warp w copies token w, and all kThreads threads
+// arrive.  Called by the threads that arrive; a no-op for an item without a
+// tile (no phase: its consumers do not wait).
 template <bool kMulti>
 __device__ __forceinline__ void refill_raw(const DecodeArgs& p, RawToken* rawt, uint64_t* bar,
                                            const Item& dn, int warp, int lane) {
   if (!dn.has_tile()) return;
   const int h = dn.hv / p.G;
   if (kMulti) {
-    const int ntok = min(1 + kWarps, dn.t1 - dn.t0);
-    for (int i = warp; i < ntok; i += kWarps) copy_raw_token(p, &rawt[i], dn.t0 + i, h, dn.hv, lane);
+    if (warp < dn.t1 - dn.t0) copy_raw_token(p, &rawt[warp], dn.t0 + warp, h, dn.hv, lane);
   } else {
     copy_raw_token(p, rawt, dn.t0, h, dn.hv, lane);
   }
   arrive_after_copies(bar);
 }
 
-// kVFirst: tiles are stored [V, K] (row v contiguous over k, the layout of a
-// transposed state); the lanes then hold runs of 4 rows of one column
-// (TileLaneT, tile_t_token_step), so tile loads and stores stay 128-bit and
-// conflict-free.  kMulti: the multi-token instance (raw buffer of 1 + kWarps
-// tokens).
-template <bool kVFirst, bool kOutBf16, bool kMulti>
+// The single-token schedule (every request has at most one token: T <= B;
+// correct for any lengths).  kVFirst: tiles are stored [V, K] (row v
+// contiguous over k, the layout of a transposed state); the lanes then hold
+// runs of 4 rows of one column (TileLaneT, tile_t_token_step), so tile loads
+// and stores stay 128-bit and conflict-free.
+template <bool kVFirst, bool kOutBf16>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const DecodeArgs p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   float* ring = reinterpret_cast<float*>(
@@ -318,11 +316,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
   using Stage = typename std::conditional<kVFirst, TokenStageT, TokenStage>::type;
   Stage* wstage = reinterpret_cast<Stage*>(ring + kBufs * kHeadDim * kHeadDim);
   RawToken* rawt = reinterpret_cast<RawToken*>(wstage + kWarps);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(rawt + (kMulti ? 1 + kWarps : 1));
-  // The raw buffer's fills (32 arrivals, warp 0's lanes; kThreads in the
-  // multi-token instance).
-  uint64_t* rawbar = bars + kBufs;
-  int3* desc = reinterpret_cast<int3*>(rawbar + 1);  // [kMaxDesc] slot, t0, t1
+  uint64_t* bars = reinterpret_cast<uint64_t*>(rawt + 1);
+  uint64_t* rawbar = bars + kBufs;  // the first-token copies (32 arrivals: warp 0's lanes)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -339,28 +334,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
     raise_status(p.dev_status, KDA_DEV_BAD_SEQLEN);
   if (threadIdx.x == 0) {
     for (int i = 0; i < kBufs; ++i) mbar_init(&bars[i], 1);
-    mbar_init(rawbar, kMulti ? kThreads : 32);
+    mbar_init(rawbar, 32);
     mbar_fence_init();
     for (int j = 0; j < kBufs && j < nmine; ++j)
       issue_item(p, load_item(p, first + j * G), first + j * G, ring + j * kHeadDim * kHeadDim,
                  &bars[j]);
   }
-  if (kMulti) {
-    for (int i = threadIdx.x; i < nmine && i < kMaxDesc; i += kThreads) {
-      const int b = (int)((first + (long long)i * G) / p.HV);
-      desc[i] = make_int3(__ldg(p.state_indices + b), __ldg(p.cu_seqlens + b),
-                          __ldg(p.cu_seqlens + b + 1));
-    }
-  }
-  __syncthreads();  // the barriers are initialised and the descriptors in place
-  if ((kMulti || warp == 0) && nmine > 0)
-    refill_raw<kMulti>(p, rawt, rawbar, get_item<kMulti>(p, desc, first, G, 0), warp, lane);
+  __syncthreads();  // the barriers are initialised
+  if (warp == 0 && nmine > 0) refill_raw<false>(p, rawt, rawbar, load_item(p, first), warp, lane);
   uint32_t rawphase = 0;  // fills of the first-token buffer consumed so far
 
   int j = 0;
   for (; j < nmine; ++j) {
     const int buf = j % kBufs;
-    const Item d = get_item<kMulti>(p, desc, first, G, j);
+    const Item d = load_item(p, first + (long long)j * G);
     const bool tile = d.has_tile();
     const int h = d.hv / p.G;
     // The item's first-token inputs, copied by warp 0 during the previous item.
@@ -393,14 +380,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
     // buffer the next item's first token.
     if (__syncthreads_or(!arrived || !raw_ok)) break;
     if (threadIdx.x == 0 && j + kBufs < nmine)
-      issue_item(p, get_item<kMulti>(p, desc, first, G, j + kBufs),
+      issue_item(p, load_item(p, first + (long long)(j + kBufs) * G),
                  first + (long long)(j + kBufs) * G, ring + buf * kHeadDim * kHeadDim, &bars[buf]);
-    // Every warp has built its record from the raw buffer: it is refilled
-    // with the next item's first token(s) -- in the multi-token instance not
-    // before this item's first round has been staged from it.
-    const bool has_round = kMulti && tile && d.t1 - d.t0 > 1;
-    if ((kMulti || warp == 0) && j + 1 < nmine && !has_round)
-      refill_raw<kMulti>(p, rawt, rawbar, get_item<kMulti>(p, desc, first, G, j + 1), warp, lane);
+    // Every warp has built its record from the raw buffer: warp 0 refills it
+    // with the next item's first token.
+    if (warp == 0 && j + 1 < nmine)
+      refill_raw<false>(p, rawt, rawbar, load_item(p, first + (long long)(j + 1) * G), warp, lane);
 
     if (!d.range_ok) {
       if (d.hv == 0 && threadIdx.x == 0) raise_status(p.dev_status, KDA_DEV_BAD_SEQLEN);
@@ -429,22 +414,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
     // every thread handles the same item.)
     for (int c0 = d.t0 + 1; c0 < d.t1; c0 += kWarps) {
       const int nc = min(kWarps, d.t1 - c0);
-      if (kMulti && c0 == d.t0 + 1) {
-        // First round: its rows came with the first token's copies.  Until
-        // now each warp has read only its own record, so it may refill it as
-        // soon as its lanes are done with it.
-        __syncwarp();
-        if (warp < nc) build_stage(p, read_raw_token(&rawt[1 + warp], lane), wstage[warp], lane);
-        __syncthreads();
-        // The raw buffer is free: refill it for the next item.
-        if (j + 1 < nmine)
-          refill_raw<kMulti>(p, rawt, rawbar, get_item<kMulti>(p, desc, first, G, j + 1), warp,
-                             lane);
-      } else {
-        __syncthreads();  // all warps are done with the records of the last round
-        if (warp < nc) build_stage(p, fetch_token(p, c0 + warp, h, d.hv, lane), wstage[warp], lane);
-        __syncthreads();
-      }
+      __syncthreads();  // all warps are done with the records of the last round
+      if (warp < nc) build_stage(p, fetch_token(p, c0 + warp, h, d.hv, lane), wstage[warp], lane);
+      __syncthreads();
       for (int jj = 0; jj < nc; ++jj) {
         const float4 o = step(s, wstage[jj], tl, tlt);
         if (kVFirst ? tlt.kq == 0 : tl.rg == 0)
@@ -475,11 +447,162 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
   }
 }
 
+
+// The multi-token schedule (some request has more than one token: T > B).
+// Per item, the first round of tokens (up to kWarps) is copied ahead into
+// the raw buffer (warp w copies token w; all kThreads threads arrive on its
+// barrier) and built at the item's start, warp w building token w's record,
+// while the tile is in flight; the CTA barrier that releases the tile slot
+// also publishes the records and frees the raw buffer, which is refilled for
+// the next item at once.  Every warp then steps through the round's records;
+// tokens past the first round are staged 8 at a time from global memory.
+// The item descriptors come from a shared table filled at kernel start.
+template <bool kVFirst, bool kOutBf16>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_multi_kernel(const DecodeArgs p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  float* ring = reinterpret_cast<float*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  using Stage = typename std::conditional<kVFirst, TokenStageT, TokenStage>::type;
+  Stage* wstage = reinterpret_cast<Stage*>(ring + kBufs * kHeadDim * kHeadDim);
+  RawToken* rawt = reinterpret_cast<RawToken*>(wstage + kWarps);  // [kWarps]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(rawt + kWarps);
+  uint64_t* rawbar = bars + kBufs;                    // kThreads arrivals per fill
+  int3* desc = reinterpret_cast<int3*>(rawbar + 1);  // [kMaxDesc] slot, t0, t1
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const TileLane tl = tile_lane();
+  const TileLaneT tlt = tile_lane_t();
+  const long long items = (long long)p.B * p.HV;
+  const long long G = gridDim.x;
+  const long long first = blockIdx.x;
+  const int nmine = items > first ? (int)((items - first + G - 1) / G) : 0;
+
+  if (blockIdx.x == 0 && threadIdx.x == 0 &&
+      (p.cu_seqlens[0] != 0 || p.cu_seqlens[p.B] != p.T))
+    raise_status(p.dev_status, KDA_DEV_BAD_SEQLEN);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kBufs; ++i) mbar_init(&bars[i], 1);
+    mbar_init(rawbar, kThreads);
+    mbar_fence_init();
+    for (int j = 0; j < kBufs && j < nmine; ++j)
+      issue_item(p, load_item(p, first + j * G), first + j * G, ring + j * kHeadDim * kHeadDim,
+                 &bars[j]);
+  }
+  for (int i = threadIdx.x; i < nmine && i < kMaxDesc; i += kThreads) {
+    const int b = (int)((first + (long long)i * G) / p.HV);
+    desc[i] = make_int3(__ldg(p.state_indices + b), __ldg(p.cu_seqlens + b),
+                        __ldg(p.cu_seqlens + b + 1));
+  }
+  __syncthreads();  // the barriers are initialised and the descriptors in place
+  if (nmine > 0) refill_raw<true>(p, rawt, rawbar, get_item<true>(p, desc, first, G, 0), warp, lane);
+  uint32_t rawphase = 0;  // fills of the raw buffer consumed so far
+
+  int j = 0;
+  for (; j < nmine; ++j) {
+    const int buf = j % kBufs;
+    const Item d = get_item<true>(p, desc, first, G, j);
+    const bool tile = d.has_tile();
+    const int h = d.hv / p.G;
+    const int n1 = min(kWarps, d.t1 - d.t0);  // tokens of the first round
+    // The first round's records, built from the raw buffer while the tile is
+    // in flight (every warp finished reading the previous item's records
+    // before that item's closing barrier).
+    bool raw_ok = true;
+    if (tile) {
+      raw_ok = mbar_wait(rawbar, rawphase & 1u, p.wait_ns);
+      ++rawphase;
+      if (warp < n1) build_stage(p, read_raw_token(&rawt[warp], lane), wstage[warp], lane);
+    }
+
+    const bool arrived = mbar_wait(&bars[buf], (uint32_t)(j / kBufs) & 1u, p.wait_ns);
+    float4 s[16];
+    if (tile && arrived) {
+      const float* src = ring + buf * kHeadDim * kHeadDim;
+      if constexpr (kVFirst) {
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            s[4 * m + c] = *reinterpret_cast<const float4*>(src + tile_t_offset(tlt, m, c));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          s[i] = *reinterpret_cast<const float4*>(src + (tl.rg + 8 * i) * kHeadDim + tl.col);
+      }
+    }
+    // Every thread has read the slot and every record of the round is built:
+    // the slot takes the tile of item j + kBufs, the raw buffer the next
+    // item's first round.
+    if (__syncthreads_or(!arrived || !raw_ok)) break;
+    if (threadIdx.x == 0 && j + kBufs < nmine)
+      issue_item(p, get_item<true>(p, desc, first, G, j + kBufs),
+                 first + (long long)(j + kBufs) * G, ring + buf * kHeadDim * kHeadDim, &bars[buf]);
+    if (j + 1 < nmine)
+      refill_raw<true>(p, rawt, rawbar, get_item<true>(p, desc, first, G, j + 1), warp, lane);
+
+    if (!d.range_ok) {
+      if (d.hv == 0 && threadIdx.x == 0) raise_status(p.dev_status, KDA_DEV_BAD_SEQLEN);
+      continue;
+    }
+    if (!d.slot_ok) {
+      if (d.slot >= p.max_slots && d.hv == 0 && threadIdx.x == 0)
+        raise_status(p.dev_status, KDA_DEV_BAD_SLOT);
+      const int quads = (d.t1 - d.t0) * (kHeadDim / 4);
+      for (int i = threadIdx.x; i < quads; i += kThreads)
+        store_out<kOutBf16>(p, d.t0 + i / (kHeadDim / 4), d.hv, (i % (kHeadDim / 4)) * 4,
+                            make_float4(0.f, 0.f, 0.f, 0.f));
+      continue;
+    }
+    if (!tile) continue;  // no tokens: the state stays bit-identical
+
+    for (int jj = 0; jj < n1; ++jj) {
+      const float4 o = step(s, wstage[jj], tl, tlt);
+      if (kVFirst ? tlt.kq == 0 : tl.rg == 0)
+        store_out<kOutBf16>(p, d.t0 + jj, d.hv, kVFirst ? tlt.col : tl.col, o);
+    }
+    // Tokens past the first round, 8 per round from global memory.
+    for (int c0 = d.t0 + kWarps; c0 < d.t1; c0 += kWarps) {
+      const int nc = min(kWarps, d.t1 - c0);
+      __syncthreads();  // all warps are done with the records of the last round
+      if (warp < nc) build_stage(p, fetch_token(p, c0 + warp, h, d.hv, lane), wstage[warp], lane);
+      __syncthreads();
+      for (int jj = 0; jj < nc; ++jj) {
+        const float4 o = step(s, wstage[jj], tl, tlt);
+        if (kVFirst ? tlt.kq == 0 : tl.rg == 0)
+          store_out<kOutBf16>(p, c0 + jj, d.hv, kVFirst ? tlt.col : tl.col, o);
+      }
+    }
+    float* dst = tile_ptr(p, d);
+    if constexpr (kVFirst) {
+      tile_t_store(dst, s, tlt);
+    } else {
+      tile_store(dst, s, tl);
+    }
+    // The next item's records overwrite this item's: every warp must be done
+    // reading them.
+    __syncthreads();
+  }
+
+  if (j < nmine) {
+    // A wait gave up: record it and let the copies already issued land
+    // (bounded) before the CTA's shared memory is released.
+    if (threadIdx.x == 0) {
+      raise_status(p.dev_status, KDA_DEV_TIMEOUT);
+      for (int k = j; k < j + kBufs && k < nmine; ++k)
+        mbar_wait(&bars[k % kBufs], (uint32_t)(k / kBufs) & 1u, p.wait_ns);
+    }
+    // The last raw-buffer fill (every thread's copies arrive on it).
+    if (rawphase > 0) mbar_wait(rawbar, (rawphase - 1) & 1u, p.wait_ns);
+    __syncthreads();
+  }
+}
+
 }  // namespace
 
 size_t decode_smem_bytes(bool multi) {
   return 128 + (size_t)kBufs * kTileBytes + kWarps * sizeof(TokenStage) +
-         (multi ? 1 + kWarps : 1) * sizeof(RawToken) + (kBufs + 1) * sizeof(uint64_t) +
+         (multi ? kWarps : 1) * sizeof(RawToken) + (kBufs + 1) * sizeof(uint64_t) +
          (multi ? kMaxDesc * sizeof(int3) : 0);
 }
 
@@ -504,16 +627,16 @@ cudaError_t launch_kda_decode(const DecodeArgs& in, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  // The multi-token instance when some request has more than one token.
+  // The multi-token schedule when some request has more than one token.
   const bool multi = args.T > args.B;
   const size_t smem = decode_smem_bytes(multi);
   void (*kernel)(DecodeArgs) =
       multi ? (args.v_first
-                   ? (args.out_bf16 ? kda_decode_kernel<true, true, true> : kda_decode_kernel<true, false, true>)
-                   : (args.out_bf16 ? kda_decode_kernel<false, true, true> : kda_decode_kernel<false, false, true>))
+                   ? (args.out_bf16 ? kda_decode_multi_kernel<true, true> : kda_decode_multi_kernel<true, false>)
+                   : (args.out_bf16 ? kda_decode_multi_kernel<false, true> : kda_decode_multi_kernel<false, false>))
             : (args.v_first
-                   ? (args.out_bf16 ? kda_decode_kernel<true, true, false> : kda_decode_kernel<true, false, false>)
-                   : (args.out_bf16 ? kda_decode_kernel<false, true, false> : kda_decode_kernel<false, false, false>));
+                   ? (args.out_bf16 ? kda_decode_kernel<true, true> : kda_decode_kernel<true, false>)
+                   : (args.out_bf16 ? kda_decode_kernel<false, true> : kda_decode_kernel<false, false>));
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const long long slots = (long long)sms * kCtasPerSm;

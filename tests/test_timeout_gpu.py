@@ -44,9 +44,12 @@ def call(lib, inp, d, out, pool, status):
                           status.data_ptr(), torch.cuda.current_stream().cuda_stream)
 
 
-def test_withheld_tile_copy_reports_timeout_and_spares_other_items():
+@pytest.mark.parametrize("tokens", [1, 2], ids=["single_token", "multi_token"])
+def test_withheld_tile_copy_reports_timeout_and_spares_other_items(tokens):
+    # one token per request: the single-token schedule; two: the multi-token one
     lib = hooks_lib()
-    inp = decode_inputs("grouped", B=64, H=4, HV=8, max_slots=80, seed=140)
+    inp = decode_inputs("grouped", B=64, H=4, HV=8, max_slots=80, seed=140,
+                        lengths=(tokens,) * 64)
     B, HV = inp["B"], inp["HV"]
     items = B * HV
     grid = min(items, 2 * torch.cuda.get_device_properties(0).multi_processor_count)
@@ -74,14 +77,16 @@ def test_withheld_tile_copy_reports_timeout_and_spares_other_items():
     got_out, got_pool = out.t.cpu().numpy(), pool.t.cpu().numpy()
     idx = inp["state_indices"].numpy()
     before = inp["state_pool"].numpy()
+    cu = inp["cu_seqlens"].numpy()
     for item in range(items):
         b, hv = divmod(item, HV)
         slot = idx[b]
+        rows = slice(cu[b], cu[b + 1])
         if item in skipped:
-            assert np.all(np.isnan(got_out[b, hv]))                       # never written
+            assert np.all(np.isnan(got_out[rows, hv]))                    # never written
             assert np.array_equal(got_pool[slot, hv], before[slot, hv])   # never stored
         else:
-            assert_outputs_close(got_out[b, hv], ref_out[b, hv])
+            assert_outputs_close(got_out[rows, hv], ref_out[rows, hv])
             assert_states_close(got_pool[slot, hv][None], ref_pool[slot, hv][None])
     # The context is still usable: the same call with no withheld item is complete.
     pool2 = guarded_copy(inp["state_pool"])
