@@ -126,6 +126,22 @@ __device__ __forceinline__ void copy_raw_token(const DecodeArgs& p, RawToken* rt
   }
 }
 
+// The same without the per-head rows (dt_bias, A_log), which the
+// multi-token schedule copies once per item (copy_raw_head).
+__device__ __forceinline__ void copy_raw_token_rows(const DecodeArgs& p, RawToken* rt, int t,
+                                                    int h, int hv, int lane) {
+  const int r0 = lane * 4;
+  cp_async_raw(&rt->q[lane], p.q + ((size_t)t * p.H + h) * kHeadDim + r0, 8);
+  cp_async_raw(&rt->k[lane], p.k + ((size_t)t * p.H + h) * kHeadDim + r0, 8);
+  cp_async_raw(&rt->v[lane], p.v + ((size_t)t * p.HV + hv) * kHeadDim + r0, 8);
+  cp_async_raw(&rt->raw[lane], p.raw_gate + ((size_t)t * p.HV + hv) * kHeadDim + r0, 16);
+  if (lane == 0) cp_async_raw(&rt->beta_logit, p.beta_logits + (size_t)t * p.HV + hv, 4);
+}
+__device__ __forceinline__ void copy_raw_head(const DecodeArgs& p, RawToken* rt, int hv, int lane) {
+  cp_async_raw(&rt->bias[lane], p.dt_bias + (size_t)hv * kHeadDim + lane * 4, 16);
+  if (lane == 0) cp_async_raw(&rt->a_log, p.a_log + hv, 4);
+}
+
 // This thread's arrival on `bar`, once all of its earlier cp.async copies
 // have completed.
 __device__ __forceinline__ void arrive_after_copies(uint64_t* bar) {
@@ -222,8 +238,9 @@ constexpr int kMaxDesc = 512;
 
 __device__ __forceinline__ Item make_item(const DecodeArgs& p, long long item, int3 st) {
   Item d;
-  d.b = (int)(item / p.HV);
-  d.hv = (int)(item - (long long)d.b * p.HV);
+  const int it = (int)item;  // B * HV < 2^31 (checked on the host)
+  d.b = it / p.HV;
+  d.hv = it - d.b * p.HV;
   d.slot = st.x;
   d.t0 = st.y;
   d.t1 = st.z;
@@ -296,7 +313,9 @@ __device__ __forceinline__ void refill_raw(const DecodeArgs& p, RawToken* rawt, 
   if (!dn.has_tile()) return;
   const int h = dn.hv / p.G;
   if (kMulti) {
-    if (warp < dn.t1 - dn.t0) copy_raw_token(p, &rawt[warp], dn.t0 + warp, h, dn.hv, lane);
+    // rawt[0] carries the item's dt_bias and A_log for every token
+    if (warp < dn.t1 - dn.t0) copy_raw_token_rows(p, &rawt[warp], dn.t0 + warp, h, dn.hv, lane);
+    if (warp == kWarps - 1) copy_raw_head(p, &rawt[0], dn.hv, lane);
   } else {
     copy_raw_token(p, rawt, dn.t0, h, dn.hv, lane);
   }
@@ -450,8 +469,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
 
 // The multi-token schedule (some request has more than one token: T > B).
 // Per item, the first round of tokens (up to kWarps) is copied ahead into
-// the raw buffer (warp w copies token w; all kThreads threads arrive on its
-// barrier) and built at the item's start, warp w building token w's record,
+// the raw buffer (warp w copies token w, the last warp the item's dt_bias
+// and A_log rows once; all kThreads threads arrive on its barrier) and built
+// at the item's start, warp w building token w's record,
 // while the tile is in flight; the CTA barrier that releases the tile slot
 // also publishes the records and frees the raw buffer, which is refilled for
 // the next item at once.  Every warp then steps through the round's records;
@@ -512,7 +532,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_multi_kernel(
     if (tile) {
       raw_ok = mbar_wait(rawbar, rawphase & 1u, p.wait_ns);
       ++rawphase;
-      if (warp < n1) build_stage(p, read_raw_token(&rawt[warp], lane), wstage[warp], lane);
+      if (warp < n1) {
+        TokenIn in = read_raw_token(&rawt[warp], lane);
+        in.bias = rawt[0].bias[lane];
+        in.a_log = rawt[0].a_log;
+        build_stage(p, in, wstage[warp], lane);
+      }
     }
 
     const bool arrived = mbar_wait(&bars[buf], (uint32_t)(j / kBufs) & 1u, p.wait_ns);
