@@ -304,9 +304,11 @@ def test_v_first_and_bf16_output_against_oracle(name, gate):
     assert torch.equal(bf_pool, vf_pool)
 
 
-def test_v_first_bf16_full_size_against_oracle():
-    # every request of the grouped workload, V-first tiles, bf16 output
-    inp = decode_inputs("grouped")
+@pytest.mark.parametrize("name", ["grouped", "varlen"])
+def test_v_first_bf16_full_size_against_oracle(name):
+    # every request of the workload, V-first tiles, bf16 output (varlen: the
+    # multi-token kernel)
+    inp = decode_inputs(name)
     out, pool = run_ex(inp, True, torch.bfloat16)
 
     def bf16_bound(got, ref):
