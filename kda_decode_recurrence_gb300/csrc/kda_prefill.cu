@@ -20,15 +20,28 @@
 // lower_bound: the bound the chunkwise prefill relies on); the softplus gate
 // has no such bound and is served by kda_decode.
 //
-// One 256-thread CTA per (request, value head); the [128, 128] state tile is
-// held in registers in the accumulator layout of the tensor-core products
-// (warp w: value columns 16w .. 16w + 15; see the FragLane comment), and the
-// three products against it per chunk run on mma.sync with split-tf32
-// operands.
+// One 256-thread CTA per (request, value head), two per SM.  The fp32
+// [128, 128] state tile stays in registers (thread (w, i) holds value column
+// v = 32 (w % 4) + i for the 64 channels of half w / 4).  The products against
+// it run on the 5th-generation tensor cores (tcgen05, accumulators in tensor
+// memory), with every fp32 operand split into three bf16 parts p0 + p1 + p2
+// (each difference exact in fp32) and the six part-products whose order is
+// at most 2 summed, which carries fp32 precision:
+//   reads   [ws | qs]^T = S0^T [kt | qt]   M = 128 values, N = 32 tokens,
+//           K = 128 channels; A = the state's parts, written to tensor memory
+//           by the threads that hold them (tcgen05.st), B = the decayed keys
+//           and queries in shared memory (K-major, 128-byte swizzle);
+//   update  S^T += u^T ke^T                M = 128 values, N = 128 channels,
+//           K = 16 tokens; A = u's parts in tensor memory, B = ke in shared
+//           memory (N-major, 128-byte swizzle); the result is read back and
+//           added to the decayed registers.
+// The A and Q products, the triangular solve and the outputs stay on the
+// CUDA cores; the outputs overlap the update's MMAs.
 #include <cstddef>
 
 #include "kda_async.cuh"
 #include "kda_recurrence.cuh"
+#include "kda_tcgen05.cuh"
 
 namespace kda {
 namespace {
@@ -39,7 +52,19 @@ constexpr int kTS = 20;    // row stride of the [channel][token] arrays: 16-byte
                            // the 8 row groups of a warp read 8 disjoint bank quads
 constexpr float kL2Eps = 1e-6f;
 
+// Tensor memory: 256 columns per CTA (two CTAs per SM use all 512).
+constexpr uint32_t kTmemCols = 256;
+constexpr int kColSParts = 0;   // 3 x 64 columns: the state's bf16 parts (A of the reads)
+constexpr int kColReads = 192;  // 32 columns: the reads' accumulator [ws | qs]
+constexpr int kColUParts = 0;   // 3 x 8 columns: u's bf16 parts (A of the update), after the reads
+constexpr int kColUpd = 32;     // 128 columns: the update's accumulator, after the reads
+
 struct PrefillSmem {
+  // B operands, 128-byte rows of 64 bf16 in the 128-byte swizzle, 1024-aligned:
+  // reads: part, channel panel (64 channels), 32 token rows (kt then qt);
+  // update: part, channel atom (64 channels), 16 token rows (ke).
+  unsigned char readsB[3][2][2 * kC * 128];
+  unsigned char updB[3][2][kC * 128];
   float qh[kC][kHeadDim];    // normalised, scaled queries   [token][channel]
   float kh[kC][kHeadDim];    // normalised keys
   float gg[kC][kHeadDim];    // log-decays
@@ -47,14 +72,13 @@ struct PrefillSmem {
   __align__(16) float ktT[kHeadDim][kTS];  // kh_t * exp(G_t)     [channel][token]
   __align__(16) float qtT[kHeadDim][kTS];  // qh_t * exp(G_t)
   __align__(16) float kbT[kHeadDim][kTS];  // kh_t * exp(-G_t)
-  __align__(16) float keT[kHeadDim][kTS];  // kh_t * exp(G_end - G_t)
   __align__(16) float eGC[kHeadDim];  // exp(G_end)
   float A[kC][kC];           // A_ts, s < t
   float Q[kC][kC];           // Q_ts, s <= t
-  __align__(16) float ws[kC][kHeadDim];  // (D_t kh_t)^T S0
-  __align__(16) float qs[kC][kHeadDim];  // (D_t qh_t)^T S0
   __align__(16) float u[kC][kHeadDim];
   float beta[kC];
+  uint64_t bar;              // MMA completion
+  uint32_t tmem_base;
 };
 
 // Token inputs a lane stages: entries 4 lane .. 4 lane + 3.
@@ -175,84 +199,41 @@ __device__ __forceinline__ void stage(const DecodeArgs& p, const ChunkIn& in, bo
   if (lane == 0) sm.beta[tt] = beta;
 }
 
-// ---- The state on the tensor cores (mma.sync m16n8k8, tf32 inputs, fp32
-// accumulation).  Warp w owns value columns v in [16w, 16w + 16); with
-// g = lane / 4 and q = lane % 4, register sf[j][e] holds S[c][v] for
-//   c = 8j + 2q + (e & 1),  v = 16w + g + 8 (e >> 1),   j = 0..15,
-// which is the accumulator fragment of S^T (rows v, columns c) for the update
-// S^T += u^T keT^T, and -- reading positions q and q + 4 of each 8-wide
-// k block as c = 8j + 2q and 8j + 2q + 1 -- the A fragment of S^T for the
-// reads ws^T = S^T kt and qs^T = S^T qt, with no data movement.  Every fp32
-// operand is split into a tf32 part and a tf32 remainder; the three products
-// hi*hi + hi*lo + lo*hi carry about 22 significant bits (the dropped lo*lo
-// term is below 2^-22 relative).
-struct FragLane {
-  int g, q, v0;  // v0 = 16w + g
-};
+// ---- bf16 parts and the 128-byte swizzle
 
-__device__ __forceinline__ FragLane frag_lane() {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  return FragLane{lane >> 2, lane & 3, 16 * warp + (lane >> 2)};
+// x = p0 + p1 + p2 as bf16 bit patterns (round to nearest; both residuals are
+// exact in fp32, so the three parts carry x to fp32 precision).
+__device__ __forceinline__ void split3(float x, uint32_t (&pt)[3]) {
+  const __nv_bfloat16 b0 = __float2bfloat16_rn(x);
+  const float r1 = x - __bfloat162float(b0);
+  const __nv_bfloat16 b1 = __float2bfloat16_rn(r1);
+  const float r2 = r1 - __bfloat162float(b1);
+  pt[0] = __bfloat16_as_ushort(b0);
+  pt[1] = __bfloat16_as_ushort(b1);
+  pt[2] = __bfloat16_as_ushort(__float2bfloat16_rn(r2));
 }
 
-__device__ __forceinline__ void frag_tile_load(float (&sf)[16][4], const float* tile, FragLane f) {
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const float* r = tile + (8 * j + 2 * f.q) * kHeadDim + f.v0;
-    sf[j][0] = __ldcs(r);
-    sf[j][1] = __ldcs(r + kHeadDim);
-    sf[j][2] = __ldcs(r + 8);
-    sf[j][3] = __ldcs(r + kHeadDim + 8);
-  }
+// Byte offset of element `col` (0..63, bf16) of row `row` in a panel of
+// 128-byte rows stored in the 128-byte swizzle (16-byte chunk index XOR row
+// mod 8; the panel is 1024-byte aligned), the layout the tensor cores read.
+__device__ __forceinline__ int sw128(int row, int col) {
+  const int byte = col * 2;
+  return row * 128 + ((((byte >> 4) ^ (row & 7)) << 4) | (byte & 15));
 }
 
-__device__ __forceinline__ void frag_tile_store(float* tile, const float (&sf)[16][4], FragLane f) {
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    float* r = tile + (8 * j + 2 * f.q) * kHeadDim + f.v0;
-    __stcs(r, sf[j][0]);
-    __stcs(r + kHeadDim, sf[j][1]);
-    __stcs(r + 8, sf[j][2]);
-    __stcs(r + kHeadDim + 8, sf[j][3]);
-  }
-}
+// The part-products summed, smallest first: (A part, B part) with
+// part(A) + part(B) <= 2.
+__constant__ int kPairs[6][2] = {{2, 0}, {1, 1}, {0, 2}, {1, 0}, {0, 1}, {0, 0}};
 
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
-
-__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
-  hi = to_tf32(x);
-  lo = to_tf32(x - __uint_as_float(hi));
-}
-
-__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// d += (ahi + alo)(bhi + blo) without the lo * lo term, small terms first.
-__device__ __forceinline__ void mma3(float (&d)[4], const uint32_t (&ahi)[4],
-                                     const uint32_t (&alo)[4], uint32_t bh0, uint32_t bh1,
-                                     uint32_t bl0, uint32_t bl1) {
-  mma_tf32(d, alo, bh0, bh1);
-  mma_tf32(d, ahi, bl0, bl1);
-  mma_tf32(d, ahi, bh0, bh1);
-}
-
-// Two CTAs per SM (128 registers, ~100 KB of shared memory each) so that a
-// batch of (request, head) items twice the SM count runs in one wave.
-// kPB: the piece size of the q, k, v copies (16 when all three pointers are
-// 16-byte aligned, else 8).
+// Two CTAs per SM (128 registers, about 110 KB of shared memory and 256
+// tensor-memory columns each), so that a batch of (request, head) items
+// twice the SM count runs in one wave.  kPB: the piece size of the q, k, v
+// copies (16 when all three pointers are 16-byte aligned, else 8).
 template <int kPB>
 __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeArgs p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  PrefillSmem& sm = *reinterpret_cast<PrefillSmem*>(smem_raw);
+  PrefillSmem& sm = *reinterpret_cast<PrefillSmem*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int item = blockIdx.x;
   const int b = item / p.HV;
@@ -279,16 +260,35 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
   }
   if (t1 == t0) return;
 
-  const FragLane fl = frag_lane();
+  // Tensor memory and the MMA completion barrier.
+  if (warp == 0) tmem_alloc(&sm.tmem_base, kTmemCols);
+  if (tid == 0) {
+    mbar_init(&sm.bar, 1);
+    mbar_fence_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const int lq = warp & 3, half = warp >> 2;
+  const int v = 32 * lq + lane;         // this thread's value column (its TMEM lane)
+  const int cbase = 64 * half;          // its channels cbase .. cbase + 63
+  const uint32_t tlane = tmem + ((uint32_t)(32 * lq) << 16);
+  const uint32_t idesc_reads = idesc_bf16(2 * kC, kHeadDim, false, false);
+  const uint32_t idesc_upd = idesc_bf16(kHeadDim, kHeadDim, false, true);
+
   float* tile = p.state_pool + ((size_t)slot * p.HV + hv) * (size_t)(kHeadDim * kHeadDim);
-  float sf[16][4];
-  frag_tile_load(sf, tile, fl);
+  float st[64];  // S[cbase + c][v]
+#pragma unroll
+  for (int c = 0; c < 64; ++c) st[c] = __ldcs(tile + (size_t)(cbase + c) * kHeadDim + v);
   const int h = hv / p.G;
   const float a_exp = expf(p.a_log[hv]);
   float* out = static_cast<float*>(p.output);
 
   unsigned char* raw = reinterpret_cast<unsigned char*>(&sm.qh[0][0]);
   const float4 bias = __ldg(reinterpret_cast<const float4*>(p.dt_bias + (size_t)hv * kHeadDim + lane * 4));
+  uint32_t mma_phase = 0;
+  bool failed = false;  // uniform: a wait on the tensor cores gave up
   issue_raw<kPB>(p, raw, t0, t1, h, hv, tid);
   for (int c0 = t0; c0 < t1; c0 += kC) {
     const int nc = min(kC, t1 - c0);
@@ -304,10 +304,12 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
       stage(p, in1, warp + 8 < nc, a_exp, sm, warp + 8, lane);
     }
     __syncthreads();
-    // ---- phase 2: cumulative decays and the decayed key/query forms.
-    // Thread c (and c + 128 for the other half of the tokens) owns channel c.
+    // ---- phase 2: cumulative decays, the decayed key/query forms (fp32 for
+    // the A and Q products, bf16 parts for the tensor cores), and the
+    // chunk-start state's parts into tensor memory.  Thread c (and c + 128
+    // for the other half of the tokens) owns channel c.
     {
-      const int c = tid & (kHeadDim - 1), half = tid >> 7;
+      const int c = tid & (kHeadDim - 1), th = tid >> 7;
       float Gt[kC];
       float G = 0.f;
 #pragma unroll
@@ -315,26 +317,74 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
         G += sm.gg[t][c];
         Gt[t] = G;
       }
+      const int pc = c >> 6, cc = c & 63;
 #pragma unroll
       for (int tt = 0; tt < kC; ++tt) {
-        if ((tt >> 3) != half) continue;  // static index into Gt, half of the tokens each
+        if ((tt >> 3) != th) continue;  // static index into Gt, half of the tokens each
         const float k = sm.kh[tt][c], q = sm.qh[tt][c];
         const float e = expf(Gt[tt]);
-        sm.ktT[c][tt] = k * e;
-        sm.qtT[c][tt] = q * e;
+        const float kt = k * e, qt = q * e, ke = k * expf(G - Gt[tt]);
+        sm.ktT[c][tt] = kt;
+        sm.qtT[c][tt] = qt;
         sm.kbT[c][tt] = k * expf(-Gt[tt]);
-        sm.keT[c][tt] = k * expf(G - Gt[tt]);
+        uint32_t pk[3], pq[3], pe[3];
+        split3(kt, pk);
+        split3(qt, pq);
+        split3(ke, pe);
+#pragma unroll
+        for (int pp = 0; pp < 3; ++pp) {
+          *reinterpret_cast<unsigned short*>(&sm.readsB[pp][pc][sw128(tt, cc)]) = (unsigned short)pk[pp];
+          *reinterpret_cast<unsigned short*>(&sm.readsB[pp][pc][sw128(kC + tt, cc)]) = (unsigned short)pq[pp];
+          *reinterpret_cast<unsigned short*>(&sm.updB[pp][pc][sw128(tt, cc)]) = (unsigned short)pe[pp];
+        }
       }
-      if (half == 0) sm.eGC[c] = expf(G);
+      if (th == 0) sm.eGC[c] = expf(G);
+      // The state's parts: column 64 part + 32 half + m of lane v holds
+      // channels cbase + 2m, cbase + 2m + 1 (K pairs, low half first).
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t r0[8], r1[8], r2[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          uint32_t lo[3], hi[3];
+          split3(st[16 * q4 + 2 * m], lo);
+          split3(st[16 * q4 + 2 * m + 1], hi);
+          r0[m] = lo[0] | (hi[0] << 16);
+          r1[m] = lo[1] | (hi[1] << 16);
+          r2[m] = lo[2] | (hi[2] << 16);
+        }
+        const uint32_t col = kColSParts + 32 * half + 8 * q4;
+        tmem_st_8cols(tlane + col, r0);
+        tmem_st_8cols(tlane + col + 64, r1);
+        tmem_st_8cols(tlane + col + 128, r2);
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();  // this thread's B-operand writes, for the tensor cores
     }
+    tc_fence_before();
     __syncthreads();
+    // ---- phase 3a: the reads [ws | qs]^T = S0^T [kt | qt] on the tensor cores
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int pr = 0; pr < 6; ++pr) {
+        const int pa = kPairs[pr][0], pb = kPairs[pr][1];
+#pragma unroll
+        for (int j = 0; j < kHeadDim / 16; ++j) {
+          const uint64_t bdesc = smem_desc_sw128(smem_u32(sm.readsB[pb][j >> 2]) + (j & 3) * 32, 16, 1024);
+          mma_bf16_tmem_a(tmem + kColReads, tmem + kColSParts + 64 * pa + 8 * j, bdesc, idesc_reads,
+                          (pr > 0 || j > 0) ? 1u : 0u);
+        }
+      }
+      mma_commit(&sm.bar);
+    }
     // qh, kh and gg are consumed: the next chunk's raw inputs start arriving there.
     if (c0 + kC < t1) issue_raw<kPB>(p, raw, c0 + kC, t1, h, hv, tid);
-    // ---- phase 3: the 16 x 16 products A (s < t) and Q (s <= t).  Thread
-    // (block of tokens t in {2tp, 2tp + 1} x s in {2sp, 2sp + 1}, channel
-    // phase cq) sums the 32 channels c = 4 cc + cq; the 4 phases (lanes
-    // 4k .. 4k + 3) are added with two xor-shuffles.  Blocks above the
-    // diagonal are zero.
+    // ---- phase 3b: the 16 x 16 products A (s < t) and Q (s <= t) on the CUDA
+    // cores while the reads run.  Thread (block of tokens t in {2tp, 2tp + 1}
+    // x s in {2sp, 2sp + 1}, channel phase cq) sums the 32 channels
+    // c = 4 cc + cq; the 4 phases (lanes 4k .. 4k + 3) are added with two
+    // xor-shuffles.  Blocks above the diagonal are zero.
     {
       const int cq = tid & 3, blk = tid >> 2, tp = blk >> 3, sp = blk & 7;
       float a[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, q[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
@@ -371,103 +421,121 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
           }
       }
     }
-    // ---- phase 4: (D_t kh_t)^T S0 and (D_t qh_t)^T S0 for the chunk, as
-    // ws^T = S0^T kt and qs^T = S0^T qt (M = the warp's 16 values, N = 16
-    // tokens in two tiles, K = the 128 channels in 16 steps of 8).
     {
-      float aw[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      float aq[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        uint32_t ahi[4], alo[4];
-        split_tf32(sf[j][0], ahi[0], alo[0]);  // (row g,     k q)     = S[8j + 2q][v0]
-        split_tf32(sf[j][2], ahi[1], alo[1]);  // (row g + 8, k q)
-        split_tf32(sf[j][1], ahi[2], alo[2]);  // (row g,     k q + 4) = S[8j + 2q + 1][v0]
-        split_tf32(sf[j][3], ahi[3], alo[3]);  // (row g + 8, k q + 4)
-        const int c = 8 * j + 2 * fl.q;
-#pragma unroll
-        for (int n = 0; n < 2; ++n) {
-          const int t = 8 * n + fl.g;  // B (k q, col g) = x[c][t], (k q + 4, col g) = x[c + 1][t]
-          uint32_t bh0, bl0, bh1, bl1;
-          split_tf32(sm.ktT[c][t], bh0, bl0);
-          split_tf32(sm.ktT[c + 1][t], bh1, bl1);
-          mma3(aw[n], ahi, alo, bh0, bh1, bl0, bl1);
-          split_tf32(sm.qtT[c][t], bh0, bl0);
-          split_tf32(sm.qtT[c + 1][t], bh1, bl1);
-          mma3(aq[n], ahi, alo, bh0, bh1, bl0, bl1);
-        }
-      }
-      // accumulator (row v, col t): (g, 2q), (g, 2q + 1), (g + 8, 2q), (g + 8, 2q + 1)
-#pragma unroll
-      for (int n = 0; n < 2; ++n) {
-        const int t = 8 * n + 2 * fl.q;
-        sm.ws[t][fl.v0] = aw[n][0];
-        sm.ws[t + 1][fl.v0] = aw[n][1];
-        sm.ws[t][fl.v0 + 8] = aw[n][2];
-        sm.ws[t + 1][fl.v0 + 8] = aw[n][3];
-        sm.qs[t][fl.v0] = aq[n][0];
-        sm.qs[t + 1][fl.v0] = aq[n][1];
-        sm.qs[t][fl.v0 + 8] = aq[n][2];
-        sm.qs[t + 1][fl.v0 + 8] = aq[n][3];
+      const bool ok = mbar_wait(&sm.bar, mma_phase & 1u);  // the reads are done
+      ++mma_phase;
+      if (__syncthreads_or(!ok)) {  // (also: A and Q are in shared memory)
+        failed = true;
+        break;
       }
     }
-    __syncthreads();
-    // ---- phase 5: the triangular solve for u, one value column per thread
+    tc_fence_after();
+    // ---- phase 4: the triangular solve for u, one value column per thread
+    // (threads 0..127: TMEM lane v = tid), reading ws straight from the
+    // reads' accumulator; u goes to shared memory (outputs) and, as bf16
+    // parts, to tensor memory (A of the update: column 8 part + m holds
+    // tokens 2m, 2m + 1).
     if (tid < kHeadDim) {
-      const int v = tid;
+      float ws[kC];
+      tmem_ld_16cols(tlane + kColReads, ws);
+      tmem_ld_wait();
       float uc[kC];
 #pragma unroll
       for (int t = 0; t < kC; ++t) {
-        float x = sm.vv[t][v] - sm.ws[t][v];
+        float x = sm.vv[t][v] - ws[t];
 #pragma unroll
         for (int s2 = 0; s2 < t; ++s2) x = fmaf(-sm.A[t][s2], uc[s2], x);
         uc[t] = sm.beta[t] * x;
         sm.u[t][v] = uc[t];
       }
+      uint32_t r0[8], r1[8], r2[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        uint32_t lo[3], hi[3];
+        split3(uc[2 * m], lo);
+        split3(uc[2 * m + 1], hi);
+        r0[m] = lo[0] | (hi[0] << 16);
+        r1[m] = lo[1] | (hi[1] << 16);
+        r2[m] = lo[2] | (hi[2] << 16);
+      }
+      tmem_st_8cols(tlane + kColUParts, r0);
+      tmem_st_8cols(tlane + kColUParts + 8, r1);
+      tmem_st_8cols(tlane + kColUParts + 16, r2);
+      tmem_st_wait();
     }
+    tc_fence_before();
     __syncthreads();
-    // ---- phase 6: outputs and the chunk-end state
+    // ---- phase 5a: the update S^T += u^T ke^T on the tensor cores
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int pr = 0; pr < 6; ++pr) {
+        const int pa = kPairs[pr][0], pb = kPairs[pr][1];
+        const uint64_t bdesc = smem_desc_sw128(smem_u32(sm.updB[pb][0]), kC * 128, 1024);
+        mma_bf16_tmem_a(tmem + kColUpd, tmem + kColUParts + 8 * pa, bdesc, idesc_upd,
+                        pr > 0 ? 1u : 0u);
+      }
+      mma_commit(&sm.bar);
+    }
+    // ---- phase 5b: outputs on the CUDA cores while the update runs: thread
+    // (v2, half h2) takes tokens 8 h2 .. 8 h2 + 7, qs from the reads'
+    // accumulator (its TMEM lane is v2)
     {
-      const int v = tid & (kHeadDim - 1), half = tid >> 7;
+      const int v2 = tid & (kHeadDim - 1), h2 = tid >> 7;
+      float qsv[kC / 2];
+      tmem_ld_8cols(tlane + kColReads + kC + (kC / 2) * h2, qsv);
+      tmem_ld_wait();
 #pragma unroll
       for (int t = 0; t < kC / 2; ++t) {
-        const int tt = half * (kC / 2) + t;
+        const int tt = h2 * (kC / 2) + t;
         if (tt < nc) {
-          float o = sm.qs[tt][v];
+          float o = qsv[t];
 #pragma unroll
-          for (int s2 = 0; s2 <= tt; ++s2) o = fmaf(sm.Q[tt][s2], sm.u[s2][v], o);
-          __stcs(out + ((size_t)(c0 + tt) * p.HV + hv) * kHeadDim + v, o);
+          for (int s2 = 0; s2 <= tt; ++s2) o = fmaf(sm.Q[tt][s2], sm.u[s2][v2], o);
+          __stcs(out + ((size_t)(c0 + tt) * p.HV + hv) * kHeadDim + v2, o);
         }
       }
     }
-    // The chunk-end state: S <- D_C S0, then S^T += u^T keT^T (M = the warp's
-    // 16 values, N = the 128 channels in 16 tiles, K = the 16 tokens in 2
-    // steps), accumulated into the state registers.
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float2 e = *reinterpret_cast<const float2*>(&sm.eGC[8 * j + 2 * fl.q]);
-      sf[j][0] *= e.x; sf[j][1] *= e.y; sf[j][2] *= e.x; sf[j][3] *= e.y;
-    }
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      const int t = 8 * kk + fl.q;
-      uint32_t ahi[4], alo[4];
-      split_tf32(sm.u[t][fl.v0], ahi[0], alo[0]);          // (row g,     k q)
-      split_tf32(sm.u[t][fl.v0 + 8], ahi[1], alo[1]);      // (row g + 8, k q)
-      split_tf32(sm.u[t + 4][fl.v0], ahi[2], alo[2]);      // (row g,     k q + 4)
-      split_tf32(sm.u[t + 4][fl.v0 + 8], ahi[3], alo[3]);  // (row g + 8, k q + 4)
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int c = 8 * j + fl.g;  // B (k q, col g) = keT[c][t], (k q + 4, col g) = keT[c][t + 4]
-        uint32_t bh0, bl0, bh1, bl1;
-        split_tf32(sm.keT[c][t], bh0, bl0);
-        split_tf32(sm.keT[c][t + 4], bh1, bl1);
-        mma3(sf[j], ahi, alo, bh0, bh1, bl0, bl1);
+    // ---- phase 6: the chunk-end state S <- D_C S0 + the update
+    {
+      const bool ok = mbar_wait(&sm.bar, mma_phase & 1u);
+      ++mma_phase;
+      if (__syncthreads_or(!ok)) {
+        failed = true;
+        break;
       }
     }
-    __syncthreads();  // the chunk's shared arrays are consumed
+    tc_fence_after();
+#pragma unroll
+    for (int q2 = 0; q2 < 2; ++q2) {
+      float up[32];
+      tmem_ld_32cols(tlane + kColUpd + cbase + 32 * q2, up);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        st[32 * q2 + i] = fmaf(st[32 * q2 + i], sm.eGC[cbase + 32 * q2 + i], up[i]);
+    }
+    tc_fence_before();
+    __syncthreads();  // the chunk's shared arrays and tensor-memory columns are free
   }
-  frag_tile_store(tile, sf, fl);
+  if (failed) {
+    // A wait on the tensor cores gave up: report it, let the copies and the
+    // MMAs issued finish (the latter bounded), and leave the state tile as it was.
+    cp_async_wait_all();
+    if (tid == 0) {
+      raise_status(p.dev_status, KDA_DEV_TIMEOUT);
+      mbar_wait(&sm.bar, (mma_phase - 1) & 1u);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 64; ++c) __stcs(tile + (size_t)(cbase + c) * kHeadDim + v, st[c]);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
 }
 
 }  // namespace
@@ -475,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
 cudaError_t launch_kda_prefill(const DecodeArgs& args, cudaStream_t stream) {
   const long long items = (long long)args.B * args.HV;
   if (items == 0) return cudaSuccess;
-  const size_t smem = sizeof(PrefillSmem);
+  const size_t smem = sizeof(PrefillSmem) + 1024;  // + alignment of the 1024-byte operands
   const bool a16 = ((reinterpret_cast<uintptr_t>(args.q) | reinterpret_cast<uintptr_t>(args.k) |
                      reinterpret_cast<uintptr_t>(args.v)) & 15) == 0;
   void (*kernel)(DecodeArgs) = a16 ? kda_prefill_kernel<16> : kda_prefill_kernel<8>;
