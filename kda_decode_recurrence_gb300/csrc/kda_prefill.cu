@@ -55,7 +55,7 @@ constexpr float kL2Eps = 1e-6f;
 // Tensor memory: 256 columns per CTA (two CTAs per SM use all 512).
 constexpr uint32_t kTmemCols = 256;
 constexpr int kColSParts = 0;   // 3 x 64 columns: the state's bf16 parts (A of the reads)
-constexpr int kColReads = 192;  // 32 columns: the reads' accumulator [ws | qs]
+constexpr int kColReads = 192;  // 2 x 32 columns: the reads' two accumulators [ws | qs]
 constexpr int kColUParts = 0;   // 3 x 8 columns: u's bf16 parts (A of the update), after the reads
 constexpr int kColUpd = 32;     // 128 columns: the update's accumulator, after the reads
 
@@ -73,11 +73,12 @@ struct PrefillSmem {
   __align__(16) float qtT[kHeadDim][kTS];  // qh_t * exp(G_t)
   __align__(16) float kbT[kHeadDim][kTS];  // kh_t * exp(-G_t)
   __align__(16) float eGC[kHeadDim];  // exp(G_end)
-  float A[kC][kC];           // A_ts, s < t
-  float Q[kC][kC];           // Q_ts, s <= t
+  __align__(16) float A[kC][kC];  // A_ts, s < t
+  __align__(16) float Q[kC][kC];  // Q_ts, s <= t
   __align__(16) float u[kC][kHeadDim];
   float beta[kC];
-  uint64_t bar;              // MMA completion
+  uint64_t bar_reads;        // the reads' MMAs are complete (two issuers)
+  uint64_t bar_upd;          // the update's MMAs are complete
   uint32_t tmem_base;
 };
 
@@ -213,6 +214,22 @@ __device__ __forceinline__ void split3(float x, uint32_t (&pt)[3]) {
   pt[2] = __bfloat16_as_ushort(__float2bfloat16_rn(r2));
 }
 
+// The same for a pair: word k holds part k of x0 (low half) and of x1
+// (high half), the packing the tensor cores read along K.
+__device__ __forceinline__ void split3_pair(float x0, float x1, uint32_t& w0, uint32_t& w1,
+                                            uint32_t& w2) {
+  const float2 m1 = make_float2(-1.f, -1.f);
+  __nv_bfloat162 b = __floats2bfloat162_rn(x0, x1);
+  w0 = *reinterpret_cast<uint32_t*>(&b);
+  float2 r = __ffma2_rn(m1, make_float2(__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xffff0000u)),
+                        make_float2(x0, x1));
+  b = __floats2bfloat162_rn(r.x, r.y);
+  w1 = *reinterpret_cast<uint32_t*>(&b);
+  r = __ffma2_rn(m1, make_float2(__uint_as_float(w1 << 16), __uint_as_float(w1 & 0xffff0000u)), r);
+  b = __floats2bfloat162_rn(r.x, r.y);
+  w2 = *reinterpret_cast<uint32_t*>(&b);
+}
+
 // Byte offset of element `col` (0..63, bf16) of row `row` in a panel of
 // 128-byte rows stored in the 128-byte swizzle (16-byte chunk index XOR row
 // mod 8; the panel is 1024-byte aligned), the layout the tensor cores read.
@@ -263,9 +280,13 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
   // Tensor memory and the MMA completion barrier.
   if (warp == 0) tmem_alloc(&sm.tmem_base, kTmemCols);
   if (tid == 0) {
-    mbar_init(&sm.bar, 1);
+    mbar_init(&sm.bar_reads, 2);
+    mbar_init(&sm.bar_upd, 1);
     mbar_fence_init();
   }
+  // A and Q above the diagonal blocks stay zero (the products write only
+  // the blocks on and below it).
+  for (int i = tid; i < 2 * kC * kC; i += kThreads) (&sm.A[0][0])[i] = 0.f;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -287,8 +308,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
 
   unsigned char* raw = reinterpret_cast<unsigned char*>(&sm.qh[0][0]);
   const float4 bias = __ldg(reinterpret_cast<const float4*>(p.dt_bias + (size_t)hv * kHeadDim + lane * 4));
-  uint32_t mma_phase = 0;
-  bool failed = false;  // uniform: a wait on the tensor cores gave up
+  uint32_t ph = 0;                // parity of this chunk's phase of both MMA barriers
+  uint64_t* failed = nullptr;     // uniform: the MMA barrier whose wait gave up
   issue_raw<kPB>(p, raw, t0, t1, h, hv, tid);
   for (int c0 = t0; c0 < t1; c0 += kC) {
     const int nc = min(kC, t1 - c0);
@@ -345,14 +366,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
       for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t r0[8], r1[8], r2[8];
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          uint32_t lo[3], hi[3];
-          split3(st[16 * q4 + 2 * m], lo);
-          split3(st[16 * q4 + 2 * m + 1], hi);
-          r0[m] = lo[0] | (hi[0] << 16);
-          r1[m] = lo[1] | (hi[1] << 16);
-          r2[m] = lo[2] | (hi[2] << 16);
-        }
+        for (int m = 0; m < 8; ++m)
+          split3_pair(st[16 * q4 + 2 * m], st[16 * q4 + 2 * m + 1], r0[m], r1[m], r2[m]);
         const uint32_t col = kColSParts + 32 * half + 8 * q4;
         tmem_st_8cols(tlane + col, r0);
         tmem_st_8cols(tlane + col + 64, r1);
@@ -363,32 +378,40 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
     }
     tc_fence_before();
     __syncthreads();
-    // ---- phase 3a: the reads [ws | qs]^T = S0^T [kt | qt] on the tensor cores
-    if (tid == 0) {
+    // ---- phase 3a: the reads [ws | qs]^T = S0^T [kt | qt] on the tensor cores.
+    // Two issuers (lane 0 of warps 0 and 1), three part-products each into
+    // an accumulator of its own: issuing is what limits these small MMAs.
+    if (tid == 0 || tid == 32) {
       tc_fence_after();
+      const int q = tid >> 5;
 #pragma unroll 1
-      for (int pr = 0; pr < 6; ++pr) {
+      for (int pr = 3 * q; pr < 3 * q + 3; ++pr) {
         const int pa = kPairs[pr][0], pb = kPairs[pr][1];
 #pragma unroll
         for (int j = 0; j < kHeadDim / 16; ++j) {
           const uint64_t bdesc = smem_desc_sw128(smem_u32(sm.readsB[pb][j >> 2]) + (j & 3) * 32, 16, 1024);
-          mma_bf16_tmem_a(tmem + kColReads, tmem + kColSParts + 64 * pa + 8 * j, bdesc, idesc_reads,
-                          (pr > 0 || j > 0) ? 1u : 0u);
+          mma_bf16_tmem_a(tmem + kColReads + 32 * q, tmem + kColSParts + 64 * pa + 8 * j, bdesc,
+                          idesc_reads, (pr > 3 * q || j > 0) ? 1u : 0u);
         }
       }
-      mma_commit(&sm.bar);
+      mma_commit(&sm.bar_reads);
     }
     // qh, kh and gg are consumed: the next chunk's raw inputs start arriving there.
     if (c0 + kC < t1) issue_raw<kPB>(p, raw, c0 + kC, t1, h, hv, tid);
     // ---- phase 3b: the 16 x 16 products A (s < t) and Q (s <= t) on the CUDA
-    // cores while the reads run.  Thread (block of tokens t in {2tp, 2tp + 1}
-    // x s in {2sp, 2sp + 1}, channel phase cq) sums the 32 channels
-    // c = 4 cc + cq; the 4 phases (lanes 4k .. 4k + 3) are added with two
-    // xor-shuffles.  Blocks above the diagonal are zero.
-    {
-      const int cq = tid & 3, blk = tid >> 2, tp = blk >> 3, sp = blk & 7;
+    // cores while the reads run, in warps 2..7 (warps 0 and 1 issue).  Thread
+    // (block of tokens t in {2tp, 2tp + 1} x s in {2sp, 2sp + 1}, sp <= tp:
+    // the 36 blocks on and below the diagonal; channel phase cq) sums the 32
+    // channels c = 4 cc + cq; the 4 phases (lanes 4k .. 4k + 3) are added
+    // with two xor-shuffles.
+    if (warp >= 2 && warp < 7) {  // whole warps: the shuffles below take every lane
+      const int cq = tid & 3, blk = (tid - 64) >> 2;
+      const bool active = blk < 36;
+      int tp = 0;
+      while ((tp + 1) * (tp + 2) / 2 <= blk) ++tp;
+      const int sp = blk - tp * (tp + 1) / 2;
       float a[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, q[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-      if (sp <= tp) {
+      if (active) {
 #pragma unroll 8
         for (int cc = 0; cc < kHeadDim / 4; ++cc) {
           const int c = 4 * cc + cq;
@@ -410,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
           q[i][j2] += __shfl_xor_sync(0xffffffffu, q[i][j2], 1);
           q[i][j2] += __shfl_xor_sync(0xffffffffu, q[i][j2], 2);
         }
-      if (cq == 0) {
+      if (active && cq == 0) {
 #pragma unroll
         for (int i = 0; i < 2; ++i)
 #pragma unroll
@@ -422,10 +445,9 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
       }
     }
     {
-      const bool ok = mbar_wait(&sm.bar, mma_phase & 1u);  // the reads are done
-      ++mma_phase;
+      const bool ok = mbar_wait(&sm.bar_reads, ph);  // the reads are done
       if (__syncthreads_or(!ok)) {  // (also: A and Q are in shared memory)
-        failed = true;
+        failed = &sm.bar_reads;
         break;
       }
     }
@@ -436,28 +458,28 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
     // parts, to tensor memory (A of the update: column 8 part + m holds
     // tokens 2m, 2m + 1).
     if (tid < kHeadDim) {
-      float ws[kC];
+      float ws[kC], ws1[kC];
       tmem_ld_16cols(tlane + kColReads, ws);
+      tmem_ld_16cols(tlane + kColReads + 32, ws1);
       tmem_ld_wait();
       float uc[kC];
 #pragma unroll
       for (int t = 0; t < kC; ++t) {
-        float x = sm.vv[t][v] - ws[t];
+        float x = sm.vv[t][v] - (ws[t] + ws1[t]);
 #pragma unroll
-        for (int s2 = 0; s2 < t; ++s2) x = fmaf(-sm.A[t][s2], uc[s2], x);
+        for (int s4 = 0; s4 < t; s4 += 4) {
+          const float4 a4 = *reinterpret_cast<const float4*>(&sm.A[t][s4]);
+          x = fmaf(-a4.x, uc[s4], x);
+          if (s4 + 1 < t) x = fmaf(-a4.y, uc[s4 + 1], x);
+          if (s4 + 2 < t) x = fmaf(-a4.z, uc[s4 + 2], x);
+          if (s4 + 3 < t) x = fmaf(-a4.w, uc[s4 + 3], x);
+        }
         uc[t] = sm.beta[t] * x;
         sm.u[t][v] = uc[t];
       }
       uint32_t r0[8], r1[8], r2[8];
 #pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        uint32_t lo[3], hi[3];
-        split3(uc[2 * m], lo);
-        split3(uc[2 * m + 1], hi);
-        r0[m] = lo[0] | (hi[0] << 16);
-        r1[m] = lo[1] | (hi[1] << 16);
-        r2[m] = lo[2] | (hi[2] << 16);
-      }
+      for (int m = 0; m < 8; ++m) split3_pair(uc[2 * m], uc[2 * m + 1], r0[m], r1[m], r2[m]);
       tmem_st_8cols(tlane + kColUParts, r0);
       tmem_st_8cols(tlane + kColUParts + 8, r1);
       tmem_st_8cols(tlane + kColUParts + 16, r2);
@@ -475,33 +497,41 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
         mma_bf16_tmem_a(tmem + kColUpd, tmem + kColUParts + 8 * pa, bdesc, idesc_upd,
                         pr > 0 ? 1u : 0u);
       }
-      mma_commit(&sm.bar);
+      mma_commit(&sm.bar_upd);
     }
     // ---- phase 5b: outputs on the CUDA cores while the update runs: thread
-    // (v2, half h2) takes tokens 8 h2 .. 8 h2 + 7, qs from the reads'
-    // accumulator (its TMEM lane is v2)
+    // (v2, half h2) takes tokens 4 h2 .. 4 h2 + 3 and 12 - 4 h2 .. 15 - 4 h2
+    // (68 terms each), qs from the reads' accumulators (its TMEM lane is v2)
     {
       const int v2 = tid & (kHeadDim - 1), h2 = tid >> 7;
-      float qsv[kC / 2];
-      tmem_ld_8cols(tlane + kColReads + kC + (kC / 2) * h2, qsv);
+      float qa[kC], qb[kC];
+      tmem_ld_16cols(tlane + kColReads + kC, qa);
+      tmem_ld_16cols(tlane + kColReads + 32 + kC, qb);
       tmem_ld_wait();
+      float uv[kC];
 #pragma unroll
-      for (int t = 0; t < kC / 2; ++t) {
-        const int tt = h2 * (kC / 2) + t;
-        if (tt < nc) {
-          float o = qsv[t];
+      for (int s2 = 0; s2 < kC; ++s2) uv[s2] = sm.u[s2][v2];
 #pragma unroll
-          for (int s2 = 0; s2 <= tt; ++s2) o = fmaf(sm.Q[tt][s2], sm.u[s2][v2], o);
-          __stcs(out + ((size_t)(c0 + tt) * p.HV + hv) * kHeadDim + v2, o);
+      for (int t = 0; t < kC; ++t) {
+        if (((t >> 2) == h2 || (t >> 2) == 3 - h2) && t < nc) {
+          float o = qa[t] + qb[t];
+#pragma unroll
+          for (int s4 = 0; s4 <= t; s4 += 4) {
+            const float4 q4 = *reinterpret_cast<const float4*>(&sm.Q[t][s4]);
+            o = fmaf(q4.x, uv[s4], o);
+            if (s4 + 1 <= t) o = fmaf(q4.y, uv[s4 + 1], o);
+            if (s4 + 2 <= t) o = fmaf(q4.z, uv[s4 + 2], o);
+            if (s4 + 3 <= t) o = fmaf(q4.w, uv[s4 + 3], o);
+          }
+          __stcs(out + ((size_t)(c0 + t) * p.HV + hv) * kHeadDim + v2, o);
         }
       }
     }
     // ---- phase 6: the chunk-end state S <- D_C S0 + the update
     {
-      const bool ok = mbar_wait(&sm.bar, mma_phase & 1u);
-      ++mma_phase;
+      const bool ok = mbar_wait(&sm.bar_upd, ph);
       if (__syncthreads_or(!ok)) {
-        failed = true;
+        failed = &sm.bar_upd;
         break;
       }
     }
@@ -517,6 +547,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
     }
     tc_fence_before();
     __syncthreads();  // the chunk's shared arrays and tensor-memory columns are free
+    ph ^= 1u;
   }
   if (failed) {
     // A wait on the tensor cores gave up: report it, let the copies and the
@@ -524,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
     cp_async_wait_all();
     if (tid == 0) {
       raise_status(p.dev_status, KDA_DEV_TIMEOUT);
-      mbar_wait(&sm.bar, (mma_phase - 1) & 1u);
+      mbar_wait(failed, ph);
     }
   } else {
 #pragma unroll
