@@ -123,33 +123,40 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 
 // Issue the copies of tokens c0 .. c0 + 15 (those before t1): the q, k, v
 // rows in PB-byte pieces (16 when all three are 16-byte aligned, else 8),
-// the gate rows in 16-byte pieces, and the 16 betas.
+// the gate rows in 16-byte pieces, and the 16 betas.  Thread tid takes
+// pieces tid, tid + 256, ...; with 256 threads that fixes its token and piece
+// within each row, so the loop is written out per round.
 template <int PB>
 __device__ __forceinline__ void issue_raw(const DecodeArgs& p, unsigned char* raw, int c0, int t1,
                                           int h, int hv, int tid) {
-  constexpr int kPieces = kHeadDim * 2 / PB;  // per bf16 row
-  constexpr int kQKV = 3 * kC * kPieces;
-  constexpr int kGate = kC * (kHeadDim * 4 / 16);
-  for (int i = tid; i < kQKV + kGate + kC; i += kThreads) {
-    if (i < kQKV) {
-      const int a = i / (kC * kPieces), j = i - a * (kC * kPieces), tt = j / kPieces;
-      const int part = j - tt * kPieces;
-      if (c0 + tt >= t1) continue;
-      const kda_bf16* base = a == 0 ? p.q : (a == 1 ? p.k : p.v);
-      const size_t row = a < 2 ? (size_t)(c0 + tt) * p.H + h : (size_t)(c0 + tt) * p.HV + hv;
-      cp_async(raw + a * kC * kHeadDim * 2 + tt * kHeadDim * 2 + part * PB,
-               base + row * kHeadDim + part * (PB / 2), PB);
-    } else if (i < kQKV + kGate) {
-      const int j = i - kQKV, tt = j >> 5, part = j & 31;
-      if (c0 + tt >= t1) continue;
-      cp_async(raw + kRawG + tt * kHeadDim * 4 + part * 16,
-               p.raw_gate + ((size_t)(c0 + tt) * p.HV + hv) * kHeadDim + part * 4, 16);
-    } else {
-      const int tt = i - kQKV - kGate;
-      if (c0 + tt >= t1) continue;
-      cp_async(raw + kRawB + tt * 4, p.beta_logits + (size_t)(c0 + tt) * p.HV + hv, 4);
+  static_assert(kThreads == 256 && kC == 16, "the piece assignment below assumes these");
+  constexpr int kRowsPerRound = kThreads * PB / (kHeadDim * 2);  // rows of one tensor per round
+  constexpr int kRounds = kC / kRowsPerRound;                     // rounds per tensor
+  const int part = tid % (kHeadDim * 2 / PB);
+  const int tq = tid / (kHeadDim * 2 / PB);
+#pragma unroll
+  for (int a = 0; a < 3; ++a) {
+    const kda_bf16* base = a == 0 ? p.q : (a == 1 ? p.k : p.v);
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+      const int tt = tq + kRowsPerRound * r;
+      if (c0 + tt < t1) {
+        const size_t row = a < 2 ? (size_t)(c0 + tt) * p.H + h : (size_t)(c0 + tt) * p.HV + hv;
+        cp_async(raw + a * kC * kHeadDim * 2 + tt * kHeadDim * 2 + part * PB,
+                 base + row * kHeadDim + part * (PB / 2), PB);
+      }
     }
   }
+  // gate rows: 32 pieces of 16 bytes, 8 rows per round
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int tt = (tid >> 5) + 8 * r, gp = tid & 31;
+    if (c0 + tt < t1)
+      cp_async(raw + kRawG + tt * kHeadDim * 4 + gp * 16,
+               p.raw_gate + ((size_t)(c0 + tt) * p.HV + hv) * kHeadDim + gp * 4, 16);
+  }
+  if (tid < kC && c0 + tid < t1)
+    cp_async(raw + kRawB + tid * 4, p.beta_logits + (size_t)(c0 + tid) * p.HV + hv, 4);
   cp_async_commit();
 }
 
@@ -166,38 +173,58 @@ __device__ __forceinline__ ChunkIn read_raw(const unsigned char* raw, float4 bia
   return in;
 }
 
-// Phase 1 for one token slot: norms, gate, beta into the [token][channel]
-// arrays (zeros for slots past the end of the request).
-__device__ __forceinline__ void stage(const DecodeArgs& p, const ChunkIn& in, bool valid, float a_exp,
-                                     PrefillSmem& sm, int tt, int lane) {
+// Phase 1 for the two token slots tt and tt + 8 of a warp: norms, gate,
+// beta into the [token][channel] arrays (zeros for slots past the end of the
+// request).  The two slots' four norm reductions are interleaved.
+__device__ __forceinline__ void stage_pair(const DecodeArgs& p, const ChunkIn& in0, const ChunkIn& in1,
+                                           bool valid0, bool valid1, float a_exp, PrefillSmem& sm,
+                                           int tt, int lane) {
   const int r0 = lane * 4;
-  float4 qv = make_float4(0.f, 0.f, 0.f, 0.f), kv = qv, gv = qv, vv = qv;
-  float beta = 0.f;
-  if (valid) {
-    const float q[4] = {bf16_lo(in.q.x), bf16_hi(in.q.x), bf16_lo(in.q.y), bf16_hi(in.q.y)};
-    const float k[4] = {bf16_lo(in.k.x), bf16_hi(in.k.x), bf16_lo(in.k.y), bf16_hi(in.k.y)};
+  const ChunkIn* ins[2] = {&in0, &in1};
+  float q[2][4], k[2][4], ss[4];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const ChunkIn& in = *ins[j];
+    q[j][0] = bf16_lo(in.q.x); q[j][1] = bf16_hi(in.q.x); q[j][2] = bf16_lo(in.q.y); q[j][3] = bf16_hi(in.q.y);
+    k[j][0] = bf16_lo(in.k.x); k[j][1] = bf16_hi(in.k.x); k[j][2] = bf16_lo(in.k.y); k[j][3] = bf16_hi(in.k.y);
     float qq = 0.f, kk = 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      qq = fmaf(q[i], q[i], qq);
-      kk = fmaf(k[i], k[i], kk);
+      qq = fmaf(q[j][i], q[j][i], qq);
+      kk = fmaf(k[j][i], k[j][i], kk);
     }
-    const float qsc = p.q_scale * rsqrtf(warp_sum(qq) + kL2Eps);
-    const float ksc = rsqrtf(warp_sum(kk) + kL2Eps);
-    qv = make_float4(q[0] * qsc, q[1] * qsc, q[2] * qsc, q[3] * qsc);
-    kv = make_float4(k[0] * ksc, k[1] * ksc, k[2] * ksc, k[3] * ksc);
-    gv = make_float4(p.lower_bound * sigmoidf_(a_exp * (in.raw.x + in.bias.x)),
-                     p.lower_bound * sigmoidf_(a_exp * (in.raw.y + in.bias.y)),
-                     p.lower_bound * sigmoidf_(a_exp * (in.raw.z + in.bias.z)),
-                     p.lower_bound * sigmoidf_(a_exp * (in.raw.w + in.bias.w)));
-    vv = make_float4(bf16_lo(in.v.x), bf16_hi(in.v.x), bf16_lo(in.v.y), bf16_hi(in.v.y));
-    beta = sigmoidf_(in.beta_logit);
+    ss[2 * j] = qq;
+    ss[2 * j + 1] = kk;
   }
-  *reinterpret_cast<float4*>(&sm.qh[tt][r0]) = qv;
-  *reinterpret_cast<float4*>(&sm.kh[tt][r0]) = kv;
-  *reinterpret_cast<float4*>(&sm.gg[tt][r0]) = gv;
-  *reinterpret_cast<float4*>(&sm.vv[tt][r0]) = vv;
-  if (lane == 0) sm.beta[tt] = beta;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], o);
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const ChunkIn& in = *ins[j];
+    const bool valid = j == 0 ? valid0 : valid1;
+    float4 qv = make_float4(0.f, 0.f, 0.f, 0.f), kv = qv, gv = qv, vv = qv;
+    float beta = 0.f;
+    if (valid) {
+      const float qsc = p.q_scale * rsqrtf(ss[2 * j] + kL2Eps);
+      const float ksc = rsqrtf(ss[2 * j + 1] + kL2Eps);
+      qv = make_float4(q[j][0] * qsc, q[j][1] * qsc, q[j][2] * qsc, q[j][3] * qsc);
+      kv = make_float4(k[j][0] * ksc, k[j][1] * ksc, k[j][2] * ksc, k[j][3] * ksc);
+      gv = make_float4(p.lower_bound * sigmoidf_(a_exp * (in.raw.x + in.bias.x)),
+                       p.lower_bound * sigmoidf_(a_exp * (in.raw.y + in.bias.y)),
+                       p.lower_bound * sigmoidf_(a_exp * (in.raw.z + in.bias.z)),
+                       p.lower_bound * sigmoidf_(a_exp * (in.raw.w + in.bias.w)));
+      vv = make_float4(bf16_lo(in.v.x), bf16_hi(in.v.x), bf16_lo(in.v.y), bf16_hi(in.v.y));
+      beta = sigmoidf_(in.beta_logit);
+    }
+    const int t = tt + 8 * j;
+    *reinterpret_cast<float4*>(&sm.qh[t][r0]) = qv;
+    *reinterpret_cast<float4*>(&sm.kh[t][r0]) = kv;
+    *reinterpret_cast<float4*>(&sm.gg[t][r0]) = gv;
+    *reinterpret_cast<float4*>(&sm.vv[t][r0]) = vv;
+    if (lane == 0) sm.beta[t] = beta;
+  }
 }
 
 // ---- bf16 parts and the 128-byte swizzle
@@ -321,8 +348,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
       if (warp < nc) in0 = read_raw(raw, bias, warp, lane);
       if (warp + 8 < nc) in1 = read_raw(raw, bias, warp + 8, lane);
       __syncthreads();  // the raw region is read: staging overwrites it
-      stage(p, in0, warp < nc, a_exp, sm, warp, lane);
-      stage(p, in1, warp + 8 < nc, a_exp, sm, warp + 8, lane);
+      stage_pair(p, in0, in1, warp < nc, warp + 8 < nc, a_exp, sm, warp, lane);
     }
     __syncthreads();
     // ---- phase 2: cumulative decays, the decayed key/query forms (fp32 for
