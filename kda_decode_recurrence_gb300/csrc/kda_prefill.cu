@@ -65,6 +65,8 @@ struct PrefillSmem {
   // update: part, channel atom (64 channels), 16 token rows (ke).
   unsigned char readsB[3][2][2 * kC * 128];
   unsigned char updB[3][2][kC * 128];
+  // outputs: part, 16 token rows t of Q[t][0..15] (32 bytes), 32-byte swizzle
+  __align__(256) unsigned char outB[3][kC * 32];
   float qh[kC][kHeadDim];    // normalised, scaled queries   [token][channel]
   float kh[kC][kHeadDim];    // normalised keys
   float gg[kC][kHeadDim];    // log-decays
@@ -74,11 +76,9 @@ struct PrefillSmem {
   __align__(16) float kbT[kHeadDim][kTS];  // kh_t * exp(-G_t)
   __align__(16) float eGC[kHeadDim];  // exp(G_end)
   __align__(16) float A[kC][kC];  // A_ts, s < t
-  __align__(16) float Q[kC][kC];  // Q_ts, s <= t
-  __align__(16) float u[kC][kHeadDim];
   float beta[kC];
   uint64_t bar_reads;        // the reads' MMAs are complete (two issuers)
-  uint64_t bar_upd;          // the update's MMAs are complete
+  uint64_t bar_upd;          // the update's and the outputs' MMAs are complete (two issuers)
   uint32_t tmem_base;
 };
 
@@ -265,6 +265,13 @@ __device__ __forceinline__ int sw128(int row, int col) {
   return row * 128 + ((((byte >> 4) ^ (row & 7)) << 4) | (byte & 15));
 }
 
+// The same in 32-byte rows (elements 0..15) and the 32-byte swizzle (16-byte
+// chunk index XOR bit 2 of the row; the panel is 256-byte aligned).
+__device__ __forceinline__ int sw32(int row, int col) {
+  const int byte = col * 2;
+  return row * 32 + ((((byte >> 4) ^ ((row >> 2) & 1)) << 4) | (byte & 15));
+}
+
 // The part-products summed, smallest first: (A part, B part) with
 // part(A) + part(B) <= 2.
 __constant__ int kPairs[6][2] = {{2, 0}, {1, 1}, {0, 2}, {1, 0}, {0, 1}, {0, 0}};
@@ -308,12 +315,14 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
   if (warp == 0) tmem_alloc(&sm.tmem_base, kTmemCols);
   if (tid == 0) {
     mbar_init(&sm.bar_reads, 2);
-    mbar_init(&sm.bar_upd, 1);
+    mbar_init(&sm.bar_upd, 2);
     mbar_fence_init();
   }
-  // A and Q above the diagonal blocks stay zero (the products write only
-  // the blocks on and below it).
-  for (int i = tid; i < 2 * kC * kC; i += kThreads) (&sm.A[0][0])[i] = 0.f;
+  // A and Q's parts above the diagonal blocks stay zero (the products write
+  // only the blocks on and below it).
+  for (int i = tid; i < kC * kC; i += kThreads) (&sm.A[0][0])[i] = 0.f;
+  for (int i = tid; i < 3 * kC * 32 / 4; i += kThreads) reinterpret_cast<uint32_t*>(&sm.outB[0][0])[i] = 0u;
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -324,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
   const uint32_t tlane = tmem + ((uint32_t)(32 * lq) << 16);
   const uint32_t idesc_reads = idesc_bf16(2 * kC, kHeadDim, false, false);
   const uint32_t idesc_upd = idesc_bf16(kHeadDim, kHeadDim, false, true);
+  const uint32_t idesc_out = idesc_bf16(kC, kHeadDim, false, false);
 
   float* tile = p.state_pool + ((size_t)slot * p.HV + hv) * (size_t)(kHeadDim * kHeadDim);
   float st[64];  // S[cbase + c][v]
@@ -466,8 +476,18 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
           for (int j2 = 0; j2 < 2; ++j2) {
             const int t = 2 * tp + i, s2 = 2 * sp + j2;
             sm.A[t][s2] = s2 < t ? a[i][j2] : 0.f;
-            sm.Q[t][s2] = s2 <= t ? q[i][j2] : 0.f;
           }
+        // Q's parts, the B operand of the outputs (K-major: row t holds Q[t][s])
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int t = 2 * tp + i, s2 = 2 * sp;
+          uint32_t w0, w1, w2;
+          split3_pair(s2 <= t ? q[i][0] : 0.f, s2 + 1 <= t ? q[i][1] : 0.f, w0, w1, w2);
+          *reinterpret_cast<uint32_t*>(&sm.outB[0][sw32(t, s2)]) = w0;
+          *reinterpret_cast<uint32_t*>(&sm.outB[1][sw32(t, s2)]) = w1;
+          *reinterpret_cast<uint32_t*>(&sm.outB[2][sw32(t, s2)]) = w2;
+        }
+        fence_proxy_async_smem();
       }
     }
     {
@@ -501,7 +521,6 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
           if (s4 + 3 < t) x = fmaf(-a4.w, uc[s4 + 3], x);
         }
         uc[t] = sm.beta[t] * x;
-        sm.u[t][v] = uc[t];
       }
       uint32_t r0[8], r1[8], r2[8];
 #pragma unroll
@@ -513,7 +532,9 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
     }
     tc_fence_before();
     __syncthreads();
-    // ---- phase 5a: the update S^T += u^T ke^T on the tensor cores
+    // ---- phase 5: the update S^T += u^T ke^T (lane 0 of warp 0) and the
+    // outputs' intra-chunk term O^T += u^T Q^T, added into the first reads
+    // accumulator's qs columns (lane 0 of warp 1), on the tensor cores
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll 1
@@ -524,36 +545,16 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
                         pr > 0 ? 1u : 0u);
       }
       mma_commit(&sm.bar_upd);
-    }
-    // ---- phase 5b: outputs on the CUDA cores while the update runs: thread
-    // (v2, half h2) takes tokens 4 h2 .. 4 h2 + 3 and 12 - 4 h2 .. 15 - 4 h2
-    // (68 terms each), qs from the reads' accumulators (its TMEM lane is v2)
-    {
-      const int v2 = tid & (kHeadDim - 1), h2 = tid >> 7;
-      float qa[kC], qb[kC];
-      tmem_ld_16cols(tlane + kColReads + kC, qa);
-      tmem_ld_16cols(tlane + kColReads + 32 + kC, qb);
-      tmem_ld_wait();
-      float uv[kC];
-#pragma unroll
-      for (int s2 = 0; s2 < kC; ++s2) uv[s2] = sm.u[s2][v2];
-#pragma unroll
-      for (int t = 0; t < kC; ++t) {
-        if (((t >> 2) == h2 || (t >> 2) == 3 - h2) && t < nc) {
-          float o = qa[t] + qb[t];
-#pragma unroll
-          for (int s4 = 0; s4 <= t; s4 += 4) {
-            const float4 q4 = *reinterpret_cast<const float4*>(&sm.Q[t][s4]);
-            o = fmaf(q4.x, uv[s4], o);
-            if (s4 + 1 <= t) o = fmaf(q4.y, uv[s4 + 1], o);
-            if (s4 + 2 <= t) o = fmaf(q4.z, uv[s4 + 2], o);
-            if (s4 + 3 <= t) o = fmaf(q4.w, uv[s4 + 3], o);
-          }
-          __stcs(out + ((size_t)(c0 + t) * p.HV + hv) * kHeadDim + v2, o);
-        }
+    } else if (tid == 32) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int pr = 0; pr < 6; ++pr) {
+        const int pa = kPairs[pr][0], pb = kPairs[pr][1];
+        const uint64_t bdesc = smem_desc_sw32(smem_u32(sm.outB[pb]), 16, 256);
+        mma_bf16_tmem_a(tmem + kColReads + kC, tmem + kColUParts + 8 * pa, bdesc, idesc_out, 1u);
       }
+      mma_commit(&sm.bar_upd);
     }
-    // ---- phase 6: the chunk-end state S <- D_C S0 + the update
     {
       const bool ok = mbar_wait(&sm.bar_upd, ph);
       if (__syncthreads_or(!ok)) {
@@ -562,6 +563,21 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
       }
     }
     tc_fence_after();
+    // ---- phase 6: outputs o_t = (both qs accumulators) for tokens
+    // 8 h2 .. 8 h2 + 7 of value column v (TMEM lane v), then the chunk-end
+    // state S <- D_C S0 + the update
+    {
+      const int h2 = tid >> 7;
+      float qa[kC / 2], qb[kC / 2];
+      tmem_ld_8cols(tlane + kColReads + kC + (kC / 2) * h2, qa);
+      tmem_ld_8cols(tlane + kColReads + 32 + kC + (kC / 2) * h2, qb);
+      tmem_ld_wait();
+#pragma unroll
+      for (int t = 0; t < kC / 2; ++t) {
+        const int tt = (kC / 2) * h2 + t;
+        if (tt < nc) __stcs(out + ((size_t)(c0 + tt) * p.HV + hv) * kHeadDim + v, qa[t] + qb[t]);
+      }
+    }
 #pragma unroll
     for (int q2 = 0; q2 < 2; ++q2) {
       float up[32];

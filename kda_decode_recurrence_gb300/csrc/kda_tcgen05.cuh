@@ -23,6 +23,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo,
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// The same for a K-major operand in the 32-byte swizzle (rows of 32 bytes,
+// 8-row groups SBO bytes apart; 256-byte aligned).
+__device__ __forceinline__ uint64_t smem_desc_sw32(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (6ull << 61);
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, the
 // major-ness of A and B, N and M.
 __device__ __forceinline__ uint32_t idesc_bf16(int n, int m, bool a_mn_major, bool b_mn_major) {
