@@ -171,8 +171,10 @@ kda_status kda_decode_ex(void* output, const kda_bf16* q, const kda_bf16* k, con
  * with a cache).  Arguments, layouts, outputs, state handling and device
  * status bits are those of kda_decode (K_FIRST state, fp32 output); the
  * result equals the token-by-token recurrence up to rounding (the products
- * against the state use split-tf32 tensor-core arithmetic, about as accurate
- * as fp32).  Meant for
+ * against the state run on the tensor cores with every fp32 operand split
+ * into three bf16 parts, about as accurate as fp32).  The device status bit
+ * KDA_DEV_TIMEOUT reports a bounded wait on the tensor cores that gave up;
+ * that request's state tile is then left unwritten.  Meant for
  * long prompts: each request's tokens are processed 16 at a time by one CTA
  * per (request, value head).
  *
