@@ -35,7 +35,7 @@ VARIANTS = {
     "outgate_swish": (os.path.join(BUILD_DIR, "libkda_outgate_swish.so"),
                       {"kda_block.cu": ["-DKDA_BLOCK_OUTPUT_GATE_SWISH=1"]}),
     "testhooks": (os.path.join(BUILD_DIR, "libkda_testhooks.so"),
-                  {"kda_decode.cu": ["-DKDA_TEST_HOOKS=1"]}),
+                  {"kda_decode.cu": ["-DKDA_TEST_HOOKS=1"], "kda_prefill.cu": ["-DKDA_TEST_HOOKS=1"]}),
 }
 
 SOURCES = ["kda_api.cu", "kda_decode.cu", "kda_block.cu", "kda_tc_gemm.cu", "kda_block_static.cu", "kda_prefill.cu"]

@@ -346,6 +346,11 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
   unsigned char* raw = reinterpret_cast<unsigned char*>(&sm.qh[0][0]);
   const float4 bias = __ldg(reinterpret_cast<const float4*>(p.dt_bias + (size_t)hv * kHeadDim + lane * 4));
   uint32_t ph = 0;                // parity of this chunk's phase of both MMA barriers
+#if KDA_TEST_HOOKS
+  const unsigned long long wait_ns = p.wait_ns;  // test-only: a shorter limit
+#else
+  constexpr unsigned long long wait_ns = kWaitLimitNs;
+#endif
   uint64_t* failed = nullptr;     // uniform: the MMA barrier whose wait gave up
   issue_raw<kPB>(p, raw, t0, t1, h, hv, tid);
   for (int c0 = t0; c0 < t1; c0 += kC) {
@@ -430,6 +435,11 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
                           idesc_reads, (pr > 3 * q || j > 0) ? 1u : 0u);
         }
       }
+#if KDA_TEST_HOOKS
+      // test-only: this item's second issuer never commits its first reads,
+      // so that phase never completes and the wait below gives up
+      if (!(q == 1 && item == p.withhold_item && c0 == t0))
+#endif
       mma_commit(&sm.bar_reads);
     }
     // qh, kh and gg are consumed: the next chunk's raw inputs start arriving there.
@@ -491,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
       }
     }
     {
-      const bool ok = mbar_wait(&sm.bar_reads, ph);  // the reads are done
+      const bool ok = mbar_wait(&sm.bar_reads, ph, wait_ns);  // the reads are done
       if (__syncthreads_or(!ok)) {  // (also: A and Q are in shared memory)
         failed = &sm.bar_reads;
         break;
@@ -556,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
       mma_commit(&sm.bar_upd);
     }
     {
-      const bool ok = mbar_wait(&sm.bar_upd, ph);
+      const bool ok = mbar_wait(&sm.bar_upd, ph, wait_ns);
       if (__syncthreads_or(!ok)) {
         failed = &sm.bar_upd;
         break;
@@ -597,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
     cp_async_wait_all();
     if (tid == 0) {
       raise_status(p.dev_status, KDA_DEV_TIMEOUT);
-      mbar_wait(failed, ph);
+      mbar_wait(failed, ph, wait_ns);
     }
   } else {
 #pragma unroll
@@ -613,7 +623,21 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
 
 }  // namespace
 
-cudaError_t launch_kda_prefill(const DecodeArgs& args, cudaStream_t stream) {
+#if KDA_TEST_HOOKS
+// Test-only build: the wait limit and the (request, head) item whose first
+// reads are never committed, for the launches that follow.
+unsigned long long g_test_prefill_wait_ns = kWaitLimitNs;
+long long g_test_prefill_withhold_item = -1;
+#endif
+
+cudaError_t launch_kda_prefill(const DecodeArgs& in, cudaStream_t stream) {
+  DecodeArgs args = in;
+  args.wait_ns = kWaitLimitNs;
+  args.withhold_item = -1;
+#if KDA_TEST_HOOKS
+  args.wait_ns = g_test_prefill_wait_ns;
+  args.withhold_item = g_test_prefill_withhold_item;
+#endif
   const long long items = (long long)args.B * args.HV;
   if (items == 0) return cudaSuccess;
   const size_t smem = sizeof(PrefillSmem) + 1024;  // + alignment of the 1024-byte operands
@@ -627,3 +651,13 @@ cudaError_t launch_kda_prefill(const DecodeArgs& args, cudaStream_t stream) {
 }
 
 }  // namespace kda
+
+#if KDA_TEST_HOOKS
+// Exported by the test-only build (libkda_testhooks.so), not declared in
+// kda.h: set the prefill kernel's wait limit and the work item (request * HV
+// + value head) whose first reads are never committed.
+extern "C" void kda_test_set_prefill_hooks(long long withhold_item, unsigned long long wait_ns) {
+  kda::g_test_prefill_withhold_item = withhold_item;
+  kda::g_test_prefill_wait_ns = wait_ns;
+}
+#endif

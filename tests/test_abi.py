@@ -46,6 +46,12 @@ def test_variant_library_exports_every_declared_symbol(lib, variant):
     assert vlib.kda_version().decode() == lib.kda_version().decode()
 
 
+def test_testhooks_variant_exports_its_hooks():
+    vlib = _lib.load_variant("testhooks")
+    for name in ("kda_test_set_decode_hooks", "kda_test_set_prefill_hooks"):
+        assert hasattr(vlib, name), name
+
+
 def test_status_strings(lib):
     for code in _lib.STATUS:
         s = lib.kda_status_string(code).decode()
