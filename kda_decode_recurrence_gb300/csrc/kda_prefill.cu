@@ -352,20 +352,24 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
   constexpr unsigned long long wait_ns = kWaitLimitNs;
 #endif
   uint64_t* failed = nullptr;     // uniform: the MMA barrier whose wait gave up
+  // Phase 1, staging a chunk's tokens (warp w takes slots w and w + 8): the
+  // first chunk here, every later one while the previous chunk's update and
+  // output MMAs run.
+  auto stage_chunk = [&](int cs) {
+    const int ns = min(kC, t1 - cs);
+    cp_async_wait_all();
+    __syncthreads();  // every thread's copies of this chunk have landed
+    ChunkIn in0 = {}, in1 = {};
+    if (warp < ns) in0 = read_raw(raw, bias, warp, lane);
+    if (warp + 8 < ns) in1 = read_raw(raw, bias, warp + 8, lane);
+    __syncthreads();  // the raw region is read: staging overwrites it
+    stage_pair(p, in0, in1, warp < ns, warp + 8 < ns, a_exp, sm, warp, lane);
+  };
   issue_raw<kPB>(p, raw, t0, t1, h, hv, tid);
+  stage_chunk(t0);
+  __syncthreads();
   for (int c0 = t0; c0 < t1; c0 += kC) {
     const int nc = min(kC, t1 - c0);
-    // ---- phase 1: stage the chunk's tokens, warp w takes slots w and w + 8
-    {
-      cp_async_wait_all();
-      __syncthreads();  // every thread's copies of this chunk have landed
-      ChunkIn in0 = {}, in1 = {};
-      if (warp < nc) in0 = read_raw(raw, bias, warp, lane);
-      if (warp + 8 < nc) in1 = read_raw(raw, bias, warp + 8, lane);
-      __syncthreads();  // the raw region is read: staging overwrites it
-      stage_pair(p, in0, in1, warp < nc, warp + 8 < nc, a_exp, sm, warp, lane);
-    }
-    __syncthreads();
     // ---- phase 2: cumulative decays, the decayed key/query forms (fp32 for
     // the A and Q products, bf16 parts for the tensor cores), and the
     // chunk-start state's parts into tensor memory.  Thread c (and c + 128
@@ -380,15 +384,17 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
         Gt[t] = G;
       }
       const int pc = c >> 6, cc = c & 63;
+      const float eG = expf(G);  // exp(G_end): ke = kb exp(G_end)
 #pragma unroll
       for (int tt = 0; tt < kC; ++tt) {
         if ((tt >> 3) != th) continue;  // static index into Gt, half of the tokens each
         const float k = sm.kh[tt][c], q = sm.qh[tt][c];
         const float e = expf(Gt[tt]);
-        const float kt = k * e, qt = q * e, ke = k * expf(G - Gt[tt]);
+        const float kb = k * expf(-Gt[tt]);
+        const float kt = k * e, qt = q * e, ke = kb * eG;
         sm.ktT[c][tt] = kt;
         sm.qtT[c][tt] = qt;
-        sm.kbT[c][tt] = k * expf(-Gt[tt]);
+        sm.kbT[c][tt] = kb;
         uint32_t pk[3], pq[3], pe[3];
         split3(kt, pk);
         split3(qt, pq);
@@ -400,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
           *reinterpret_cast<unsigned short*>(&sm.updB[pp][pc][sw128(tt, cc)]) = (unsigned short)pe[pp];
         }
       }
-      if (th == 0) sm.eGC[c] = expf(G);
+      if (th == 0) sm.eGC[c] = eG;
       // The state's parts: column 64 part + 32 half + m of lane v holds
       // channels cbase + 2m, cbase + 2m + 1 (K pairs, low half first).
 #pragma unroll
@@ -565,6 +571,9 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
       }
       mma_commit(&sm.bar_upd);
     }
+    // The next chunk's staging while those MMAs run (its copies were issued
+    // in phase 3; vv and beta of this chunk were last read by the solve).
+    if (c0 + kC < t1) stage_chunk(c0 + kC);
     {
       const bool ok = mbar_wait(&sm.bar_upd, ph, wait_ns);
       if (__syncthreads_or(!ok)) {
