@@ -34,9 +34,16 @@
 //   update  S^T += u^T ke^T                M = 128 values, N = 128 channels,
 //           K = 16 tokens; A = u's parts in tensor memory, B = ke in shared
 //           memory (N-major, 128-byte swizzle); the result is read back and
-//           added to the decayed registers.
-// The A and Q products, the triangular solve and the outputs stay on the
-// CUDA cores; the outputs overlap the update's MMAs.
+//           added to the decayed registers;
+//   outputs O^T = qs + u^T Q^T             M = 128 values, N = 16 tokens,
+//           K = 16 tokens; A = u's parts, B = Q's parts in shared memory
+//           (K-major, 32-byte swizzle), accumulated onto the reads' qs.
+// Each tcgen05.mma of these shapes costs its issuing thread about 90 cycles,
+// so the reads are issued by two threads into two accumulators (three
+// part-products each, summed when read back), and the update and the outputs
+// by one thread each.  The A and Q products and the triangular solve stay on
+// the CUDA cores: A and Q beside the reads' issue, and the next chunk's
+// staging beside the update and output MMAs.
 #include <cstddef>
 
 #include "kda_async.cuh"
@@ -48,8 +55,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kC = 16;     // tokens per chunk
-constexpr int kTS = 20;    // row stride of the [channel][token] arrays: 16-byte aligned, and
-                           // the 8 row groups of a warp read 8 disjoint bank quads
+constexpr int kTS = 20;    // row stride of the [channel][token] arrays (16-byte aligned rows)
 constexpr float kL2Eps = 1e-6f;
 
 // Tensor memory: 256 columns per CTA (two CTAs per SM use all 512).
