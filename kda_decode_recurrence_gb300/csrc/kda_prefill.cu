@@ -280,7 +280,27 @@ __device__ __forceinline__ int sw32(int row, int col) {
 
 // The part-products summed, smallest first: (A part, B part) with
 // part(A) + part(B) <= 2.
-__constant__ int kPairs[6][2] = {{2, 0}, {1, 1}, {0, 2}, {1, 0}, {0, 1}, {0, 0}};
+// Pair pr (0..5): (2, 0), (1, 1), (0, 2), (1, 0), (0, 1), (0, 0).
+__host__ __device__ constexpr int part_a(int pr) { return pr == 0 ? 2 : (pr == 1 || pr == 3) ? 1 : 0; }
+__host__ __device__ constexpr int part_b(int pr) { return pr == 2 ? 2 : (pr == 1 || pr == 4) ? 1 : 0; }
+
+// The reads' MMAs of issuer Q (part-products 3Q .. 3Q + 2, into accumulator
+// Q), written out so that every descriptor is a constant offset from one base.
+template <int Q>
+__device__ __forceinline__ void issue_reads(uint32_t readsB_addr, uint32_t tmem, uint32_t idesc) {
+  const uint64_t base = smem_desc_sw128(readsB_addr, 16, 1024);
+#pragma unroll
+  for (int i = 0; i < 3; ++i) {
+#pragma unroll
+    for (int j = 0; j < kHeadDim / 16; ++j) {
+      const int pr = 3 * Q + i;
+      // readsB[part][channel panel] is 4096 bytes; a K step of 16 is 32 bytes
+      const uint32_t off = (uint32_t)((part_b(pr) * 2 + (j >> 2)) * (2 * kC * 128) + (j & 3) * 32);
+      mma_bf16_tmem_a(tmem + kColReads + 32 * Q, tmem + kColSParts + 64 * part_a(pr) + 8 * j,
+                      base + (off >> 4), idesc, (i > 0 || j > 0) ? 1u : 0u);
+    }
+  }
+}
 
 // Two CTAs per SM (128 registers, about 110 KB of shared memory and 256
 // tensor-memory columns each), so that a batch of (request, head) items
@@ -437,16 +457,10 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
     if (tid == 0 || tid == 32) {
       tc_fence_after();
       const int q = tid >> 5;
-#pragma unroll 1
-      for (int pr = 3 * q; pr < 3 * q + 3; ++pr) {
-        const int pa = kPairs[pr][0], pb = kPairs[pr][1];
-#pragma unroll
-        for (int j = 0; j < kHeadDim / 16; ++j) {
-          const uint64_t bdesc = smem_desc_sw128(smem_u32(sm.readsB[pb][j >> 2]) + (j & 3) * 32, 16, 1024);
-          mma_bf16_tmem_a(tmem + kColReads + 32 * q, tmem + kColSParts + 64 * pa + 8 * j, bdesc,
-                          idesc_reads, (pr > 3 * q || j > 0) ? 1u : 0u);
-        }
-      }
+      if (q == 0)
+        issue_reads<0>(smem_u32(&sm.readsB[0][0][0]), tmem, idesc_reads);
+      else
+        issue_reads<1>(smem_u32(&sm.readsB[0][0][0]), tmem, idesc_reads);
 #if KDA_TEST_HOOKS
       // test-only: this item's second issuer never commits its first reads,
       // so that phase never completes and the wait below gives up
@@ -559,22 +573,19 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
     // accumulator's qs columns (lane 0 of warp 1), on the tensor cores
     if (tid == 0) {
       tc_fence_after();
-#pragma unroll 1
-      for (int pr = 0; pr < 6; ++pr) {
-        const int pa = kPairs[pr][0], pb = kPairs[pr][1];
-        const uint64_t bdesc = smem_desc_sw128(smem_u32(sm.updB[pb][0]), kC * 128, 1024);
-        mma_bf16_tmem_a(tmem + kColUpd, tmem + kColUParts + 8 * pa, bdesc, idesc_upd,
-                        pr > 0 ? 1u : 0u);
-      }
+      const uint64_t base = smem_desc_sw128(smem_u32(&sm.updB[0][0][0]), kC * 128, 1024);
+#pragma unroll
+      for (int pr = 0; pr < 6; ++pr)  // updB[part] is 4096 bytes
+        mma_bf16_tmem_a(tmem + kColUpd, tmem + kColUParts + 8 * part_a(pr),
+                        base + ((part_b(pr) * 2 * kC * 128) >> 4), idesc_upd, pr > 0 ? 1u : 0u);
       mma_commit(&sm.bar_upd);
     } else if (tid == 32) {
       tc_fence_after();
-#pragma unroll 1
-      for (int pr = 0; pr < 6; ++pr) {
-        const int pa = kPairs[pr][0], pb = kPairs[pr][1];
-        const uint64_t bdesc = smem_desc_sw32(smem_u32(sm.outB[pb]), 16, 256);
-        mma_bf16_tmem_a(tmem + kColReads + kC, tmem + kColUParts + 8 * pa, bdesc, idesc_out, 1u);
-      }
+      const uint64_t base = smem_desc_sw32(smem_u32(&sm.outB[0][0]), 16, 256);
+#pragma unroll
+      for (int pr = 0; pr < 6; ++pr)  // outB[part] is 512 bytes
+        mma_bf16_tmem_a(tmem + kColReads + kC, tmem + kColUParts + 8 * part_a(pr),
+                        base + ((part_b(pr) * kC * 32) >> 4), idesc_out, 1u);
       mma_commit(&sm.bar_upd);
     }
     // The next chunk's staging while those MMAs run (its copies were issued
