@@ -37,13 +37,32 @@ def check(inp, bs=None, state_tol=1e-5):
                         ref_pool, tol=state_tol)
 
 
-@pytest.mark.parametrize("lb", [-5.0, -1.0])
+@pytest.mark.parametrize("lb", [-5.0, -1.0, 0.0])
 def test_chunk_boundaries_against_oracle(lb):
+    # lb = 0: every g is 0, no decay at all (the degenerate end of the gate)
     # partial chunks, exactly one chunk, one past a chunk, several chunks
     inp = decode_inputs("varlen", B=6, H=2, HV=4, max_slots=8,
                         lengths=(1, 15, 16, 17, 40, 100), seed=120)
     inp["lower_bound"] = lb
     check(inp)
+
+
+def test_many_ragged_requests_with_empty_ones():
+    # one launch over requests of very different chunk counts, some of them
+    # empty: every request and head against the oracle, the empty requests'
+    # tiles bit-identical
+    rng = np.random.default_rng(126)
+    lengths = [int(x) for x in rng.integers(0, 150, size=24)]
+    lengths[3] = lengths[11] = lengths[20] = 0
+    inp = decode_inputs("varlen", B=24, H=4, HV=8, max_slots=30, lengths=tuple(lengths), seed=126)
+    out, pool, st = gpu_prefill(inp)
+    assert st == 0
+    idx = inp["state_indices"].numpy()
+    for b in (3, 11, 20):
+        assert torch.equal(pool[int(idx[b])].cpu(), inp["state_pool"][int(idx[b])])
+    rows, slots, ref_out, ref_pool = oracle_decode_sample(inp, list(range(24)))
+    assert_outputs_close(out.cpu().numpy()[rows], ref_out)
+    assert_states_close(pool[torch.from_numpy(slots.astype(np.int64)).cuda()].cpu().numpy(), ref_pool)
 
 
 def test_long_sequence_against_oracle():
