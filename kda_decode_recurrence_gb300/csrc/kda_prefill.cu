@@ -91,7 +91,7 @@ struct PrefillSmem {
 // Token inputs a lane stages: entries 4 lane .. 4 lane + 3.
 struct ChunkIn {
   uint2 q, k, v;
-  float4 raw, bias;
+  float4 raw;
   float beta_logit;
 };
 
@@ -168,13 +168,12 @@ __device__ __forceinline__ void issue_raw(const DecodeArgs& p, unsigned char* ra
 
 
 // Token slot tt's inputs for lane `lane` (entries 4 lane .. 4 lane + 3) from the raw region.
-__device__ __forceinline__ ChunkIn read_raw(const unsigned char* raw, float4 bias, int tt, int lane) {
+__device__ __forceinline__ ChunkIn read_raw(const unsigned char* raw, int tt, int lane) {
   ChunkIn in;
   in.q = *reinterpret_cast<const uint2*>(raw + kRawQ + tt * kHeadDim * 2 + lane * 8);
   in.k = *reinterpret_cast<const uint2*>(raw + kRawK + tt * kHeadDim * 2 + lane * 8);
   in.v = *reinterpret_cast<const uint2*>(raw + kRawV + tt * kHeadDim * 2 + lane * 8);
   in.raw = *reinterpret_cast<const float4*>(raw + kRawG + tt * kHeadDim * 4 + lane * 16);
-  in.bias = bias;
   in.beta_logit = *reinterpret_cast<const float*>(raw + kRawB + tt * 4);
   return in;
 }
@@ -183,9 +182,13 @@ __device__ __forceinline__ ChunkIn read_raw(const unsigned char* raw, float4 bia
 // beta into the [token][channel] arrays (zeros for slots past the end of the
 // request).  The two slots' four norm reductions are interleaved.
 __device__ __forceinline__ void stage_pair(const DecodeArgs& p, const ChunkIn& in0, const ChunkIn& in1,
-                                           bool valid0, bool valid1, float a_exp, PrefillSmem& sm,
+                                           bool valid0, bool valid1, int hv, PrefillSmem& sm,
                                            int tt, int lane) {
   const int r0 = lane * 4;
+  // per-head gate parameters, read here (cache hits) rather than held in
+  // registers across the chunk loop
+  const float a_exp = expf(__ldg(p.a_log + hv));
+  const float4 bias = __ldg(reinterpret_cast<const float4*>(p.dt_bias + (size_t)hv * kHeadDim + r0));
   const ChunkIn* ins[2] = {&in0, &in1};
   float q[2][4], k[2][4], ss[4];
 #pragma unroll
@@ -217,10 +220,10 @@ __device__ __forceinline__ void stage_pair(const DecodeArgs& p, const ChunkIn& i
       const float ksc = rsqrtf(ss[2 * j + 1] + kL2Eps);
       qv = make_float4(q[j][0] * qsc, q[j][1] * qsc, q[j][2] * qsc, q[j][3] * qsc);
       kv = make_float4(k[j][0] * ksc, k[j][1] * ksc, k[j][2] * ksc, k[j][3] * ksc);
-      gv = make_float4(p.lower_bound * sigmoidf_(a_exp * (in.raw.x + in.bias.x)),
-                       p.lower_bound * sigmoidf_(a_exp * (in.raw.y + in.bias.y)),
-                       p.lower_bound * sigmoidf_(a_exp * (in.raw.z + in.bias.z)),
-                       p.lower_bound * sigmoidf_(a_exp * (in.raw.w + in.bias.w)));
+      gv = make_float4(p.lower_bound * sigmoidf_(a_exp * (in.raw.x + bias.x)),
+                       p.lower_bound * sigmoidf_(a_exp * (in.raw.y + bias.y)),
+                       p.lower_bound * sigmoidf_(a_exp * (in.raw.z + bias.z)),
+                       p.lower_bound * sigmoidf_(a_exp * (in.raw.w + bias.w)));
       vv = make_float4(bf16_lo(in.v.x), bf16_hi(in.v.x), bf16_lo(in.v.y), bf16_hi(in.v.y));
       beta = sigmoidf_(in.beta_logit);
     }
@@ -366,11 +369,9 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
 #pragma unroll
   for (int c = 0; c < 64; ++c) st[c] = __ldcs(tile + (size_t)(cbase + c) * kHeadDim + v);
   const int h = hv / p.G;
-  const float a_exp = expf(p.a_log[hv]);
   float* out = static_cast<float*>(p.output);
 
   unsigned char* raw = reinterpret_cast<unsigned char*>(&sm.qh[0][0]);
-  const float4 bias = __ldg(reinterpret_cast<const float4*>(p.dt_bias + (size_t)hv * kHeadDim + lane * 4));
   uint32_t ph = 0;                // parity of this chunk's phase of both MMA barriers
 #if KDA_TEST_HOOKS
   const unsigned long long wait_ns = p.wait_ns;  // test-only: a shorter limit
@@ -386,10 +387,10 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
     cp_async_wait_all();
     __syncthreads();  // every thread's copies of this chunk have landed
     ChunkIn in0 = {}, in1 = {};
-    if (warp < ns) in0 = read_raw(raw, bias, warp, lane);
-    if (warp + 8 < ns) in1 = read_raw(raw, bias, warp + 8, lane);
+    if (warp < ns) in0 = read_raw(raw, warp, lane);
+    if (warp + 8 < ns) in1 = read_raw(raw, warp + 8, lane);
     __syncthreads();  // the raw region is read: staging overwrites it
-    stage_pair(p, in0, in1, warp < ns, warp + 8 < ns, a_exp, sm, warp, lane);
+    stage_pair(p, in0, in1, warp < ns, warp + 8 < ns, hv, sm, warp, lane);
   };
   issue_raw<kPB>(p, raw, t0, t1, h, hv, tid);
   stage_chunk(t0);
