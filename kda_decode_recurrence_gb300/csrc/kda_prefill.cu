@@ -87,6 +87,9 @@ struct PrefillSmem {
   uint64_t bar_upd;          // the update's and the outputs' MMAs are complete (two issuers)
   uint32_t tmem_base;
 };
+// Two CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per
+// CTA, and 1 KB of alignment slack per CTA for the 1024-byte operands.
+static_assert(2 * (sizeof(PrefillSmem) + 1024 + 1024) <= 228 * 1024, "two prefill CTAs fit an SM");
 
 // Token inputs a lane stages: entries 4 lane .. 4 lane + 3.
 struct ChunkIn {
