@@ -145,3 +145,36 @@ def test_gates_outside_the_chunk_form_run_the_token_kernel(gate, lb):
     assert st_p == 0 and st_d == 0
     assert torch.equal(out_p, out_d) and torch.equal(pool_p, pool_d)
     check(inp)
+
+
+def test_prefill_then_decode_steps_equal_one_pass():
+    # the serving flow: a prompt prefilled in chunks, then tokens decoded one
+    # call each on the same pool, against the oracle over all the tokens
+    P, steps = 70, 3
+    inp = decode_inputs("varlen", B=3, H=2, HV=4, max_slots=5, lengths=(P + steps,) * 3, seed=127)
+    d = to_device(inp)
+    B, HV = inp["B"], inp["HV"]
+    T = P + steps
+    tok = {k: d[k].view(B, T, *d[k].shape[1:]) for k in ("q", "k", "v", "raw_gate", "beta_logits")}
+    pool = d["state_pool"].clone()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.full((B, T, HV, 128), float("nan"), device="cuda")
+    seg = lambda name, a, b: tok[name][:, a:b].reshape(-1, *tok[name].shape[2:]).contiguous()
+    cu = lambda n: torch.arange(0, B * n + 1, n, dtype=torch.int32, device="cuda")
+    o = torch.empty(B * P, HV, 128, device="cuda")
+    kda_prefill(o, seg("q", 0, P), seg("k", 0, P), seg("v", 0, P), seg("raw_gate", 0, P),
+                seg("beta_logits", 0, P), d["a_log"], d["dt_bias"], cu(P), pool, d["state_indices"],
+                gate_mode=inp["gate_mode"], lower_bound=inp["lower_bound"], dev_status=status)
+    out[:, :P] = o.view(B, P, HV, 128)
+    for j in range(P, T):
+        o1 = torch.empty(B, HV, 128, device="cuda")
+        kda_decode(o1, seg("q", j, j + 1), seg("k", j, j + 1), seg("v", j, j + 1),
+                   seg("raw_gate", j, j + 1), seg("beta_logits", j, j + 1), d["a_log"], d["dt_bias"],
+                   cu(1), pool, d["state_indices"], gate_mode=inp["gate_mode"],
+                   lower_bound=inp["lower_bound"], dev_status=status)
+        out[:, j] = o1
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rows, slots, ref_out, ref_pool = oracle_decode_sample(inp, list(range(B)))
+    assert_outputs_close(out.view(B * T, HV, 128).cpu().numpy()[rows], ref_out)
+    assert_states_close(pool[torch.from_numpy(slots.astype(np.int64)).cuda()].cpu().numpy(), ref_pool)
