@@ -147,6 +147,23 @@ def test_gates_outside_the_chunk_form_run_the_token_kernel(gate, lb):
     check(inp)
 
 
+def test_many_waves_of_ctas_match_the_token_kernel():
+    # 64 requests x 96 heads = 6144 CTAs, about 20 waves at two per SM: every
+    # wave allocates and frees its tensor memory; the results equal the
+    # token-by-token kernel's within the bounds, and a sample the oracle's
+    inp = decode_inputs("varlen", B=64, H=96, HV=96, max_slots=128, seed=128,
+                        lengths=tuple(int(x) for x in np.random.default_rng(128).integers(1, 100, 64)))
+    out_c, pool_c, st_c = gpu_prefill(inp)
+    out_r, pool_r, st_r = gpu_prefill(inp, fn=kda_decode)
+    assert st_c == 0 and st_r == 0
+    assert_outputs_close(out_c.cpu().numpy(), out_r.cpu().double().numpy(), "out")
+    slots = inp["state_indices"].long().cuda()
+    assert_states_close(pool_c[slots].cpu().numpy(), pool_r[slots].cpu().double().numpy(), "S")
+    rows, sl, ref_out, ref_pool = oracle_decode_sample(inp, [0, 31, 63])
+    assert_outputs_close(out_c.cpu().numpy()[rows], ref_out)
+    assert_states_close(pool_c[torch.from_numpy(sl.astype(np.int64)).cuda()].cpu().numpy(), ref_pool)
+
+
 def test_prefill_then_decode_steps_equal_one_pass():
     # the serving flow: a prompt prefilled in chunks, then tokens decoded one
     # call each on the same pool, against the oracle over all the tokens
