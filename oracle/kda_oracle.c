@@ -77,7 +77,8 @@ static double gate_value(double raw, double dt_bias, double a_log, int gate_mode
  * for the gate.  Reading: the logistic sigmoid (the same squashing the page
  * uses for the forget gate), with z * sigmoid(z) (swish) as the documented
  * alternative.  Pinned per setting by closed forms at z = 0 and z >> 0 in
- * the test suite; which of the two the page means is parity unpinned. */
+ * the test suite; which of the two the page means is a reading the page
+ * leaves open (sigmoid is the default). */
 static double output_gate(double z, int out_gate) {
   if (out_gate == ORACLE_OUT_GATE_SWISH) return z * sigmoid(z);
   return sigmoid(z);
@@ -145,7 +146,8 @@ static void delta_rule_token(double* S, double* o, const double* qh, const doubl
  *   cu[0] != 0 or cu[B] != T sets ORACLE_BAD_SEQLEN only.
  *
  * Parity: pinned by the delta-rule properties, closed forms and brute force in
- * the test suite; the gate formula itself is unpinned (see gate_value). */
+ * the test suite; the gate formula by the closed forms its wording fixes (see
+ * gate_value). */
 int oracle_kda_decode(double* output, const double* q, const double* k, const double* v,
                       const double* raw_gate, const double* beta_logits, const double* a_log,
                       const double* dt_bias, const int32_t* cu_seqlens, double* state_pool,
