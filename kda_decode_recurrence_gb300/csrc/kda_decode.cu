@@ -232,13 +232,17 @@ __device__ __forceinline__ Item load_item(const DecodeArgs& p, long long item) {
   return d;
 }
 
-// Descriptors kept in shared memory per CTA (slot, t0, t1 of its items j <
-// kMaxDesc); items beyond are read from global memory.
+// Descriptors kept in shared memory per CTA (slot, t0, t1 and the item
+// index b * HV + hv of its items j < kMaxDesc); items beyond are read from
+// global memory.
 constexpr int kMaxDesc = 512;
+// The multi-token schedule balances its CTAs' work when B is at most this
+// (every CTA ranks the requests by length at its start).
+constexpr int kMaxRankB = 1024;
 
-__device__ __forceinline__ Item make_item(const DecodeArgs& p, long long item, int3 st) {
+__device__ __forceinline__ Item make_item(const DecodeArgs& p, int4 st) {
   Item d;
-  const int it = (int)item;  // B * HV < 2^31 (checked on the host)
+  const int it = st.w;  // B * HV < 2^31 (checked on the host)
   d.b = it / p.HV;
   d.hv = it - d.b * p.HV;
   d.slot = st.x;
@@ -249,13 +253,17 @@ __device__ __forceinline__ Item make_item(const DecodeArgs& p, long long item, i
   return d;
 }
 
-// Item j of this CTA (global index first + j * G): from the shared table in
-// the multi-token instance, else from global memory.
+// Item j of this CTA: from the shared table in the multi-token instance
+// (which also holds its index), else global index first + j * G, from
+// global memory.
 template <bool kMulti>
-__device__ __forceinline__ Item get_item(const DecodeArgs& p, const int3* desc, long long first,
+__device__ __forceinline__ Item get_item(const DecodeArgs& p, const int4* desc, long long first,
                                          long long G, int j) {
-  const long long item = first + (long long)j * G;
-  return kMulti && j < kMaxDesc ? make_item(p, item, desc[j]) : load_item(p, item);
+  return kMulti && j < kMaxDesc ? make_item(p, desc[j]) : load_item(p, first + (long long)j * G);
+}
+__device__ __forceinline__ long long item_index(const int4* desc, long long first, long long G,
+                                                int j) {
+  return j < kMaxDesc ? (long long)desc[j].w : first + (long long)j * G;
 }
 
 __device__ __forceinline__ float* tile_ptr(const DecodeArgs& p, const Item& d) {
@@ -487,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_multi_kernel(
   RawToken* rawt = reinterpret_cast<RawToken*>(wstage + kWarps);  // [kWarps]
   uint64_t* bars = reinterpret_cast<uint64_t*>(rawt + kWarps);
   uint64_t* rawbar = bars + kBufs;                    // kThreads arrivals per fill
-  int3* desc = reinterpret_cast<int3*>(rawbar + 1);  // [kMaxDesc] slot, t0, t1
+  int4* desc = reinterpret_cast<int4*>(rawbar + 1);  // [kMaxDesc] slot, t0, t1, item
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -496,25 +504,64 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_multi_kernel(
   const long long items = (long long)p.B * p.HV;
   const long long G = gridDim.x;
   const long long first = blockIdx.x;
-  const int nmine = items > first ? (int)((items - first + G - 1) / G) : 0;
+  // Work balance: an item costs a fixed part plus a part per token, and the
+  // kernel lasts as long as its busiest CTA.  When the requests can be ranked
+  // at the start (B <= kMaxRankB) and every CTA's list fits the table, the
+  // items are taken in order of their request's length, longest first (ties
+  // by request), and dealt to the CTAs in a serpentine: round r gives
+  // position r G + i to CTA i when r is even and to CTA G - 1 - i when it is
+  // odd.  Otherwise CTA c takes items c, c + G, c + 2G, ...  Which CTA
+  // computes an item does not change its result.
+  const bool balanced = p.B <= kMaxRankB && (items + G - 1) / G <= kMaxDesc;
+  int nmine;
+  if (balanced) {
+    const long long R = items / G, rem = items - R * G;
+    nmine = (int)R + (int)((R & 1) == 0 ? first < rem : G - 1 - first < rem);
+  } else {
+    nmine = items > first ? (int)((items - first + G - 1) / G) : 0;
+  }
 
   if (blockIdx.x == 0 && threadIdx.x == 0 &&
       (p.cu_seqlens[0] != 0 || p.cu_seqlens[p.B] != p.T))
     raise_status(p.dev_status, KDA_DEV_BAD_SEQLEN);
+  // The requests' ranks, in the tile slot (free until the first tile is issued).
+  int* len_s = reinterpret_cast<int*>(ring);  // [B] token counts
+  int* order = len_s + kMaxRankB;             // [B] rank -> request
+  if (balanced) {
+    for (int b = threadIdx.x; b < p.B; b += kThreads)
+      len_s[b] = __ldg(p.cu_seqlens + b + 1) - __ldg(p.cu_seqlens + b);
+    __syncthreads();
+    for (int b = threadIdx.x; b < p.B; b += kThreads) {
+      const int nb = len_s[b];
+      int r = 0;
+      for (int b2 = 0; b2 < p.B; ++b2) {
+        const int n2 = len_s[b2];
+        r += (n2 > nb || (n2 == nb && b2 < b)) ? 1 : 0;
+      }
+      order[r] = b;
+    }
+    __syncthreads();
+  }
+  for (int i = threadIdx.x; i < nmine && i < kMaxDesc; i += kThreads) {
+    long long item = first + (long long)i * G;
+    if (balanced) {
+      const long long pos = (long long)i * G + ((i & 1) == 0 ? first : G - 1 - first);
+      item = (long long)order[pos / p.HV] * p.HV + pos % p.HV;
+    }
+    const int b = (int)(item / p.HV);
+    desc[i] = make_int4(__ldg(p.state_indices + b), __ldg(p.cu_seqlens + b),
+                        __ldg(p.cu_seqlens + b + 1), (int)item);
+  }
+  __syncthreads();  // the descriptors are in place and the slot is free again
   if (threadIdx.x == 0) {
     for (int i = 0; i < kBufs; ++i) mbar_init(&bars[i], 1);
     mbar_init(rawbar, kThreads);
     mbar_fence_init();
     for (int j = 0; j < kBufs && j < nmine; ++j)
-      issue_item(p, load_item(p, first + j * G), first + j * G, ring + j * kHeadDim * kHeadDim,
-                 &bars[j]);
+      issue_item(p, get_item<true>(p, desc, first, G, j), item_index(desc, first, G, j),
+                 ring + j * kHeadDim * kHeadDim, &bars[j]);
   }
-  for (int i = threadIdx.x; i < nmine && i < kMaxDesc; i += kThreads) {
-    const int b = (int)((first + (long long)i * G) / p.HV);
-    desc[i] = make_int3(__ldg(p.state_indices + b), __ldg(p.cu_seqlens + b),
-                        __ldg(p.cu_seqlens + b + 1));
-  }
-  __syncthreads();  // the barriers are initialised and the descriptors in place
+  __syncthreads();  // the barriers are initialised
   if (nmine > 0) refill_raw<true>(p, rawt, rawbar, get_item<true>(p, desc, first, G, 0), warp, lane);
   uint32_t rawphase = 0;  // fills of the raw buffer consumed so far
 
@@ -562,7 +609,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_multi_kernel(
     if (__syncthreads_or(!arrived || !raw_ok)) break;
     if (threadIdx.x == 0 && j + kBufs < nmine)
       issue_item(p, get_item<true>(p, desc, first, G, j + kBufs),
-                 first + (long long)(j + kBufs) * G, ring + buf * kHeadDim * kHeadDim, &bars[buf]);
+                 item_index(desc, first, G, j + kBufs), ring + buf * kHeadDim * kHeadDim,
+                 &bars[buf]);
     if (j + 1 < nmine)
       refill_raw<true>(p, rawt, rawbar, get_item<true>(p, desc, first, G, j + 1), warp, lane);
 
@@ -628,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_multi_kernel(
 size_t decode_smem_bytes(bool multi) {
   return 128 + (size_t)kBufs * kTileBytes + kWarps * sizeof(TokenStage) +
          (multi ? kWarps : 1) * sizeof(RawToken) + (kBufs + 1) * sizeof(uint64_t) +
-         (multi ? kMaxDesc * sizeof(int3) : 0);
+         (multi ? kMaxDesc * sizeof(int4) : 0);
 }
 
 #if KDA_TEST_HOOKS

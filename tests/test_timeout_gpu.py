@@ -60,7 +60,17 @@ def test_withheld_tile_copy_reports_timeout_and_spares_other_items(tokens):
     grid = min(items, 2 * torch.cuda.get_device_properties(0).multi_processor_count)
     withheld = 5
     # the CTA owning the withheld item fails on it and skips it and its later items
-    skipped = set(range(withheld, items, grid))
+    if tokens == 1:
+        skipped = set(range(withheld, items, grid))  # CTA c takes items c, c + G, ...
+    else:
+        # the multi-token kernel deals the items, ordered by request length
+        # (all equal here, so by index), to the CTAs in a serpentine
+        def owned(c):
+            R, rem = divmod(items, grid)
+            n = R + ((c < rem) if R % 2 == 0 else (grid - 1 - c < rem))
+            return [j * grid + (c if j % 2 == 0 else grid - 1 - c) for j in range(n)]
+        mine = next(owned(c) for c in range(grid) if withheld in owned(c))
+        skipped = set(mine[mine.index(withheld):])
     d = to_device(inp)
     pool = guarded_copy(inp["state_pool"])
     out = Guarded((inp["T"], HV, 128), torch.float32, fill=float("nan"))
