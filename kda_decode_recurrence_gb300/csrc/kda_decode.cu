@@ -8,7 +8,9 @@
 // GB300 design (HBM-bound: 64 KiB in + 64 KiB out per tile, ~1 flop/byte):
 //   * a persistent grid, two 256-thread CTAs per SM (128 registers each, so
 //     16 warps per SM hide each other's latency); CTA c takes the (request,
-//     value head) work items c, c + G, c + 2G, ... (G = grid size);
+//     value head) work items c, c + G, c + 2G, ... (G = grid size), except in
+//     the multi-token instance, which deals the items ordered by request
+//     length in a serpentine so that every CTA gets the same work;
 //   * each tile is fetched with one 64 KiB bulk copy (cp.async.bulk, the
 //     non-tensor TMA path) into the CTA's shared-memory slot as soon as the
 //     previous tile has moved into registers, so the next tile is in flight
