@@ -79,6 +79,10 @@ typedef enum kda_status {
                                 cu[B] != T: a request with a bad range is skipped              */
 #define KDA_DEV_TIMEOUT 4    /* an internal copy/tensor-core pipeline wait exceeded its 1 s limit;
                                 the kernel stopped early and its results are incomplete          */
+#define KDA_DEV_BOUNDS 8     /* debug builds only (libkda_debugbounds.so, compiled with
+                                KDA_DEBUG_BOUNDS=1): an index the kernels derived fell outside
+                                its tensor; that access was skipped.  Never set by libkda.so,
+                                whose kernels carry no such checks.                              */
 
 /*
  * kda_decode -- advance each request's recurrent state over its new tokens.

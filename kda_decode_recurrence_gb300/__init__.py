@@ -37,6 +37,7 @@ OUTPUT_BF16 = 1
 DEV_BAD_SLOT = 1
 DEV_BAD_SEQLEN = 2
 DEV_TIMEOUT = 4
+DEV_BOUNDS = 8  # debug builds only (libkda_debugbounds.so)
 
 
 class KdaError(RuntimeError):
@@ -51,7 +52,8 @@ class KdaDeviceError(RuntimeError):
         self.bits = bits
         names = [n for b, n in ((DEV_BAD_SLOT, "KDA_DEV_BAD_SLOT"),
                                 (DEV_BAD_SEQLEN, "KDA_DEV_BAD_SEQLEN"),
-                                (DEV_TIMEOUT, "KDA_DEV_TIMEOUT")) if bits & b]
+                                (DEV_TIMEOUT, "KDA_DEV_TIMEOUT"),
+                                (DEV_BOUNDS, "KDA_DEV_BOUNDS")) if bits & b]
         super().__init__(f"{what}: device status {bits} ({' | '.join(names) or 'unknown bits'})")
 
 

@@ -34,6 +34,9 @@ LIB_PATH = os.path.join(BUILD_DIR, "libkda.so")
 VARIANTS = {
     "outgate_swish": (os.path.join(BUILD_DIR, "libkda_outgate_swish.so"),
                       {"kda_block.cu": ["-DKDA_BLOCK_OUTPUT_GATE_SWISH=1"]}),
+    "debugbounds": (os.path.join(BUILD_DIR, "libkda_debugbounds.so"),
+                    {f: ["-DKDA_DEBUG_BOUNDS=1"] for f in ("kda_decode.cu", "kda_prefill.cu",
+                                                          "kda_block.cu")}),
     "testhooks": (os.path.join(BUILD_DIR, "libkda_testhooks.so"),
                   {"kda_decode.cu": ["-DKDA_TEST_HOOKS=1"], "kda_prefill.cu": ["-DKDA_TEST_HOOKS=1"]}),
 }

@@ -317,6 +317,7 @@ struct PrepArgs {
   const float* gamma_o;
   TokenStage* stage;  // [R, nh]
   float* zgate;       // [R, nh, V]: gamma_o[d] * output_gate(z)
+  int32_t* status;    // device status word (debug builds' index checks)
   float scale, lower_bound, l2_eps;
   int R, n, I, KS1, nh, Kc, CQ, CV, TN;
 };
@@ -457,6 +458,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) block_prep_kernel(const PrepA
     const float qsc = p.scale * rsqrtf(sq + p.l2_eps);
     const float ksc = rsqrtf(sk + p.l2_eps);
     const float beta = sigmoidf_(bl);
+    if (!kda_in_bounds(r < p.R && h < p.nh && cq < p.CQ && cv < p.CV, p.status)) continue;
     TokenStage& st = p.stage[(size_t)r * p.nh + h];
     const float kh = kv * ksc;
     st.row[d].kh = kh;
@@ -471,6 +473,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) block_prep_kernel(const PrepA
 #pragma unroll 1
   for (int j = 0; j < p.n; ++j) {
     const int r = b * p.n + j;
+    if (!kda_in_bounds(r < p.R && h < p.nh, p.status)) continue;
     const size_t gzrow = (size_t)r * (p.CQ + p.CV);
     const float graw = p.gz[gzrow + (size_t)h * kHeadDim + d];   // W_fb head-outer
     const float zz = p.gz[gzrow + p.CQ + (size_t)d * p.nh + h];  // W_gb channel-outer
@@ -488,6 +491,7 @@ struct RecArgs {
   const float* zgate;
   float* S;
   __nv_bfloat16* on2;  // [2R, CV] bf16 hi rows then lo rows
+  int32_t* status;     // device status word (debug builds' index checks)
   float rms_norm_eps;
   int R, n, nh, CV;
 };
@@ -509,6 +513,8 @@ __global__ void __launch_bounds__(kThreads, 2) block_recurrence_kernel(const Rec
   const int b = bh / p.nh, h = bh - b * p.nh;
   const int tid = threadIdx.x;
   const TileLane tl = tile_lane();
+  // debug builds: the CTA's request and head lie in the block's rows
+  if (!kda_in_bounds(b * (kMulti ? p.n : 1) < p.R && h < p.nh, p.status)) return;
 
   float* tile = p.S + (size_t)bh * (size_t)(kHeadDim * kHeadDim);
   float4 s[16];
@@ -617,6 +623,7 @@ cudaError_t launch_kda_block(const BlockArgs& a, cudaStream_t stream) {
   pa.gamma_o = a.gamma_o;
   pa.stage = stage;
   pa.zgate = zgate;
+  pa.status = err;
   pa.scale = a.scale;
   pa.lower_bound = a.lower_bound;
   pa.l2_eps = a.l2_eps;
@@ -636,6 +643,7 @@ cudaError_t launch_kda_block(const BlockArgs& a, cudaStream_t stream) {
   ra.zgate = zgate;
   ra.S = a.S;
   ra.on2 = on2;
+  ra.status = err;
   ra.rms_norm_eps = a.rms_norm_eps;
   ra.R = L.R;
   ra.n = a.n;

@@ -41,4 +41,19 @@ __device__ __forceinline__ void raise_status(int32_t* status, int32_t bit) {
   if (status != nullptr) atomicOr(status, bit);
 }
 
+// Index checks of the debug build (compiled with KDA_DEBUG_BOUNDS=1, the
+// library libkda_debugbounds.so): kda_in_bounds(cond, status) is cond, and
+// when cond fails it also sets KDA_DEV_BOUNDS, so that the caller skips the
+// access it guards.  In every other build it is the constant true and the
+// checks compile away.  (compute-sanitizer is not available everywhere these
+// kernels run; the debug build is the stand-in.)
+#if KDA_DEBUG_BOUNDS
+__device__ __forceinline__ bool kda_in_bounds(bool cond, int32_t* status) {
+  if (!cond) raise_status(status, KDA_DEV_BOUNDS);
+  return cond;
+}
+#else
+__device__ __forceinline__ constexpr bool kda_in_bounds(bool, int32_t*) { return true; }
+#endif
+
 }  // namespace kda

@@ -75,6 +75,8 @@ struct TokenIn {
 
 __device__ __forceinline__ TokenIn fetch_token(const DecodeArgs& p, int t, int h, int hv, int lane) {
   const int r0 = lane * 4;
+  if (!kda_in_bounds(t >= 0 && t < p.T && h >= 0 && h < p.H && hv >= 0 && hv < p.HV, p.dev_status))
+    return TokenIn{};
   TokenIn in;
   in.q = __ldg(reinterpret_cast<const uint2*>(p.q + ((size_t)t * p.H + h) * kHeadDim + r0));
   in.k = __ldg(reinterpret_cast<const uint2*>(p.k + ((size_t)t * p.H + h) * kHeadDim + r0));
@@ -116,6 +118,8 @@ __device__ __forceinline__ void cp_async_raw(void* dst, const void* src, int byt
 // into rt.
 __device__ __forceinline__ void copy_raw_token(const DecodeArgs& p, RawToken* rt, int t, int h,
                                                int hv, int lane) {
+  if (!kda_in_bounds(t >= 0 && t < p.T && h >= 0 && h < p.H && hv >= 0 && hv < p.HV, p.dev_status))
+    return;
   const int r0 = lane * 4;
   cp_async_raw(&rt->q[lane], p.q + ((size_t)t * p.H + h) * kHeadDim + r0, 8);
   cp_async_raw(&rt->k[lane], p.k + ((size_t)t * p.H + h) * kHeadDim + r0, 8);
@@ -132,6 +136,8 @@ __device__ __forceinline__ void copy_raw_token(const DecodeArgs& p, RawToken* rt
 // multi-token schedule copies once per item (copy_raw_head).
 __device__ __forceinline__ void copy_raw_token_rows(const DecodeArgs& p, RawToken* rt, int t,
                                                     int h, int hv, int lane) {
+  if (!kda_in_bounds(t >= 0 && t < p.T && h >= 0 && h < p.H && hv >= 0 && hv < p.HV, p.dev_status))
+    return;
   const int r0 = lane * 4;
   cp_async_raw(&rt->q[lane], p.q + ((size_t)t * p.H + h) * kHeadDim + r0, 8);
   cp_async_raw(&rt->k[lane], p.k + ((size_t)t * p.H + h) * kHeadDim + r0, 8);
@@ -272,6 +278,14 @@ __device__ __forceinline__ float* tile_ptr(const DecodeArgs& p, const Item& d) {
   return p.state_pool + ((size_t)d.slot * p.HV + d.hv) * (size_t)(kHeadDim * kHeadDim);
 }
 
+// Debug builds: the item's request, value head, key head and slot lie in
+// their tensors (always true in other builds).
+__device__ __forceinline__ bool item_in_bounds(const DecodeArgs& p, const Item& d) {
+  return kda_in_bounds(d.b >= 0 && d.b < p.B && d.hv >= 0 && d.hv < p.HV && d.hv / p.G < p.H &&
+                           d.slot >= 0 && d.slot < p.max_slots,
+                       p.dev_status);
+}
+
 // Arrive on the ring slot for item d (global index `item`) and start its
 // tile copy when it has one.
 __device__ __forceinline__ void issue_item(const DecodeArgs& p, const Item& d, long long item,
@@ -281,7 +295,7 @@ __device__ __forceinline__ void issue_item(const DecodeArgs& p, const Item& d, l
 #else
   (void)item;
 #endif
-  const bool copy = d.has_tile();
+  const bool copy = d.has_tile() && item_in_bounds(p, d);
   mbar_expect_tx(bar, copy ? kTileBytes : 0u);
   if (copy) bulk_load(dst, tile_ptr(p, d), kTileBytes, bar);
 }
@@ -298,6 +312,9 @@ __device__ __forceinline__ float4 step(float4 (&s)[16], const TokenStageT& ts, T
 // Output row of token t, value head hv: 4 consecutive values from column col.
 template <bool kOutBf16>
 __device__ __forceinline__ void store_out(const DecodeArgs& p, int t, int hv, int col, float4 o) {
+  if (!kda_in_bounds(t >= 0 && t < p.T && hv >= 0 && hv < p.HV && col >= 0 && col + 4 <= kHeadDim,
+                     p.dev_status))
+    return;
   const size_t off = ((size_t)t * p.HV + hv) * kHeadDim + col;
   if (kOutBf16) {
     const __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y);
@@ -455,11 +472,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_kernel(const 
     // The next item's first record goes into wstage[warp]: wait until every
     // warp has finished reading this item's rounds.
     if (d.t1 - d.t0 > 1) __syncthreads();
-    float* dst = tile_ptr(p, d);
-    if constexpr (kVFirst) {
-      tile_t_store(dst, s, tlt);
-    } else {
-      tile_store(dst, s, tl);
+    if (item_in_bounds(p, d)) {
+      float* dst = tile_ptr(p, d);
+      if constexpr (kVFirst) {
+        tile_t_store(dst, s, tlt);
+      } else {
+        tile_store(dst, s, tl);
+      }
     }
   }
 
@@ -648,11 +667,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kda_decode_multi_kernel(
           store_out<kOutBf16>(p, c0 + jj, d.hv, kVFirst ? tlt.col : tl.col, o);
       }
     }
-    float* dst = tile_ptr(p, d);
-    if constexpr (kVFirst) {
-      tile_t_store(dst, s, tlt);
-    } else {
-      tile_store(dst, s, tl);
+    if (item_in_bounds(p, d)) {
+      float* dst = tile_ptr(p, d);
+      if constexpr (kVFirst) {
+        tile_t_store(dst, s, tlt);
+      } else {
+        tile_store(dst, s, tl);
+      }
     }
     // The next item's records overwrite this item's: every warp must be done
     // reading them.

@@ -149,7 +149,7 @@ __device__ __forceinline__ void issue_raw(const DecodeArgs& p, unsigned char* ra
 #pragma unroll
     for (int r = 0; r < kRounds; ++r) {
       const int tt = tq + kRowsPerRound * r;
-      if (c0 + tt < t1) {
+      if (c0 + tt < t1 && kda_in_bounds(c0 + tt < p.T, p.dev_status)) {
         const size_t row = a < 2 ? (size_t)(c0 + tt) * p.H + h : (size_t)(c0 + tt) * p.HV + hv;
         cp_async(raw + a * kC * kHeadDim * 2 + tt * kHeadDim * 2 + part * PB,
                  base + row * kHeadDim + part * (PB / 2), PB);
@@ -342,6 +342,9 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
     return;
   }
   if (t1 == t0) return;
+  // debug builds: the item's request, heads and slot lie in their tensors
+  if (!kda_in_bounds(b < p.B && hv < p.HV && hv / p.G < p.H && slot < p.max_slots, p.dev_status))
+    return;
 
   // Tensor memory and the MMA completion barrier.
   if (warp == 0) tmem_alloc(&sm.tmem_base, kTmemCols);
@@ -615,7 +618,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prefill_kernel(const DecodeAr
 #pragma unroll
       for (int t = 0; t < kC / 2; ++t) {
         const int tt = (kC / 2) * h2 + t;
-        if (tt < nc) __stcs(out + ((size_t)(c0 + tt) * p.HV + hv) * kHeadDim + v, qa[t] + qb[t]);
+        if (tt < nc && kda_in_bounds(c0 + tt < p.T, p.dev_status))
+          __stcs(out + ((size_t)(c0 + tt) * p.HV + hv) * kHeadDim + v, qa[t] + qb[t]);
       }
     }
 #pragma unroll
