@@ -49,8 +49,8 @@ FALLBACK_HBM_GBS = 6800.0
 # and scaled to the full launch: reads x 8; writes x 8 less what is still
 # dirty in L2 when the kernel ends (the reduced case's algorithmic writes
 # minus its measured ones, 55.2 MB), which does not grow with the workload.
-NCU_REDUCED = {"read": 204658176, "write": 147724032, "algorithmic_write": 202899456, "scale": 8}
-NCU_TRAFFIC = {"sources_sha256": "689470db4ee01cb9b48212a11d2b8e22a80e7bb8abfc2f2aacc24406f068ceef",
+NCU_REDUCED = {"read": 204660992, "write": 147660544, "algorithmic_write": 202899456, "scale": 8}
+NCU_TRAFFIC = {"sources_sha256": "ad45e14dfdb5a47ad6fe947108b664dbad52393d5635ff7dbb9604994e466120",
                "bytes_per_launch": (NCU_REDUCED["read"] * NCU_REDUCED["scale"]
                                     + NCU_REDUCED["algorithmic_write"] * NCU_REDUCED["scale"]
                                     - (NCU_REDUCED["algorithmic_write"] - NCU_REDUCED["write"]))}
