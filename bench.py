@@ -722,9 +722,10 @@ def run_profile_case(args, which: str):
     """A reduced case for ncu captures: the decode kernel on B = 32 requests x
     1 token, H = 48, HV = 96 (a 64-slot, 400 MB pool; 200 MB of state traffic
     per launch, above the L2 size), with K-first tiles ("decode") or V-first
-    tiles ("decode_vfirst", fp32 output), or the block at its full size with
-    n = 1 or 4 tokens per request ("block", "block_n4"; "*_eager": eager calls
-    only, no CUDA graph).
+    tiles ("decode_vfirst", fp32 output), the full varlen workload (64
+    requests of 1..8 tokens, the multi-token kernel: "varlen"), or the block at
+    its full size with n = 1 or 4 tokens per request ("block", "block_n4";
+    "*_eager": eager calls only, no CUDA graph).
     Prints the median kernel time only."""
     from kda_decode_recurrence_gb300 import STATE_V_FIRST, kda_decode_ex
     dev = torch.device("cuda", 0)
@@ -739,7 +740,10 @@ def run_profile_case(args, which: str):
     if which == "prefill":
         print(json.dumps({"profile": "prefill", **run_prefill(args.steps, args.warmup)}))
         return
-    inp = decode_inputs(DECODE_CONFIGS[WORKLOAD], B=32, max_slots=64)
+    if which == "varlen":
+        inp = decode_inputs(DECODE_CONFIGS["varlen"])
+    else:
+        inp = decode_inputs(DECODE_CONFIGS[WORKLOAD], B=32, max_slots=64)
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     out = torch.empty(inp["T"], inp["HV"], inp["V"], device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -764,7 +768,7 @@ def run_profile_case(args, which: str):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile", choices=["decode", "decode_vfirst", "block", "block_n4",
+    ap.add_argument("--profile", choices=["decode", "decode_vfirst", "varlen", "block", "block_n4",
                                           "block_eager", "block_n4_eager", "prefill"],
                     default=None,
                     help="run a reduced case of one kernel for ncu (no JSON bench line)")
